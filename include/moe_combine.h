@@ -1,0 +1,199 @@
+/*
+ * moe_combine.h -- C ABI of the single-GPU MoE combine/finalize step
+ * (GB300, sm_103a).
+ *
+ * The library turns per-expert output rows, stored grouped by expert, back
+ * into per-token hidden states:
+ *
+ *   routing build   topk_ids [T, k] -> counts [E], offsets [E+1],
+ *                   row_map [T, k], src_row [N_valid]
+ *   combine         s[t]  = sum_j w[t, j] * expert_out[row_map[t, j]]  (fp32, ascending j)
+ *                           + shared_out[t]                             (optional, weight 1)
+ *                   x[t]  = s[t] + residual[t]                          (optional)
+ *                   y[t]  = x[t] / sqrt(mean(x[t]^2) + eps) * (gamma + weight_bias)  (optional)
+ *                   quant = MXFP8 (e4m3, UE8M0 per 32) or NVFP4 (e2m1, e4m3 per 16,
+ *                           global scale g) of y, scales linear or 128x4-swizzled
+ *
+ * Sources (page title -- section):
+ *  - Struct_ep_combine_skip_a2a -- execute: weighted sum of routed expert
+ *    outputs per token; args router_weights [num_tokens, top_k], topk_ids
+ *    [num_tokens, top_k], src_info (originating token of each received row),
+ *    recv_count_ptrs (tokens received per expert); parameter
+ *    fused_shared_expert (adds the shared expert's output); parameter
+ *    has_epilogue_fusion (elementwise epilogue after the combined output).
+ *  - flashinfer.megamoe.nvfp4_mega_moe -- parameters num_tokens (padding
+ *    rows are routed to -1), cumulative_local_expert_recv_stats (int32
+ *    receive count per expert), y (caller-owned output, first num_tokens
+ *    rows written in place); Notes (contiguous tensors on the device).
+ *  - flashinfer.comm.trtllm_moe_allreduce_fusion -- residual_in,
+ *    residual_out, rms_gamma, rms_eps, weight_bias (None -> 0.0, 1.0 -> the
+ *    Gemma form (1 + gamma)), scale_factor, norm_out, quant_out, scale_out,
+ *    layout_code; each output tensor is optional.
+ *  - flashinfer.comm.moe_a2a_combine -- output_dtype (bf16 or
+ *    float8_e4m3fn), output_scales (UE8M0 in uint8, vector size 32),
+ *    output_scalar_scale (per-tensor global scale applied before FP4 block
+ *    scaling), sf_layout (linear by default, or swizzled), output
+ *    (caller-provided, contiguous, same device).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named "device" are CUDA device pointers owned by the caller;
+ *    the library allocates nothing and keeps no state between calls.
+ *  - All work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and returns without synchronising, except
+ *    moe_build_row_map_check, which synchronises `stream`.
+ *  - Arguments are validated on the host before anything is launched; an
+ *    invalid call returns an error status and enqueues nothing.
+ *  - A failed kernel launch returns MOE_ERR_CUDA.
+ *  - Inputs must be finite (no NaN / Inf); they are not checked.
+ */
+#ifndef MOE_COMBINE_H
+#define MOE_COMBINE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+/* Limits of this implementation (validated on the host). */
+#define MOE_MAX_TOP_K 32
+#define MOE_MAX_EXPERTS 8192
+#define MOE_MAX_HIDDEN 16384
+
+/* cudaStream_t without including the CUDA headers (same type). */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,    /* null / misaligned pointer, bad size or enum */
+    MOE_ERR_UNSUPPORTED = 2,    /* valid request outside this build's limits */
+    MOE_ERR_WORKSPACE = 3,      /* workspace missing or too small */
+    MOE_ERR_INVALID_EXPERT = 4, /* a topk id outside [-1, E) (device-detected) */
+    MOE_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed */
+    MOE_ERR_ROW_OUT_OF_RANGE = 6, /* a row_map entry >= n_expert_rows (device-detected) */
+    MOE_ERR_DEVICE_TIMEOUT = 7  /* a bounded device-side wait gave up (device-detected) */
+} moe_status;
+
+typedef enum {
+    MOE_QUANT_NONE = 0,
+    MOE_QUANT_MXFP8 = 1, /* e4m3 codes [T, H] bytes + UE8M0 scale per 32 elements */
+    MOE_QUANT_NVFP4 = 2  /* e2m1 codes [T, H/2] bytes (element 2i in the low nibble)
+                            + e4m3 scale per 16 elements, with global scale g */
+} moe_quant_kind;
+
+typedef enum {
+    MOE_SF_LINEAR = 0,         /* scale (row r, column c) at byte r*C + c */
+    MOE_SF_SWIZZLED_128x4 = 1  /* 128-row x 4-column tiles of 512 bytes, tiles in
+                                  row-tile-major order, column tiles fastest; inside a
+                                  tile (r%32)*16 + ((r%128)/32)*4 + c%4.  Rows padded
+                                  to a multiple of 128, columns to a multiple of 4;
+                                  the library writes the pad bytes as 0. */
+} moe_sf_layout;
+
+/* MOE_ABI_VERSION of the loaded library. */
+int moe_abi_version(void);
+
+/* A static, human-readable name for a moe_status value. */
+const char *moe_status_string(int status);
+
+/* sizeof(moe_combine_args) as compiled into the library (ABI check). */
+size_t moe_combine_args_size(void);
+
+/* ------------------------------------------------------------------------
+ * Routing build (Struct_ep_combine_skip_a2a: topk_ids, src_info,
+ * recv_count_ptrs; nvfp4_mega_moe: num_tokens padding with -1,
+ * cumulative_local_expert_recv_stats).
+ *
+ * Given topk_ids (int32, [T, top_k] row-major, device), computes
+ *   counts[e]    number of slots routed to expert e              int32 [E]
+ *   offsets[e]   sum of counts[e'] for e' < e; offsets[E] = N_valid  int32 [E+1]
+ *   row_map[t,j] row of the expert-grouped buffer holding token t's output
+ *                from slot j: offsets[e] + the number of earlier slots
+ *                (t', j') < (t, j), in row-major order, routed to the same
+ *                expert e; -1 for a padded slot                    int32 [T, top_k]
+ *   src_row[r]   t * top_k + j of the slot stored in row r, for r < N_valid
+ *                (optional, NULL to skip; capacity T * top_k)     int32
+ * The result is unique and deterministic (bit-identical across runs).
+ * An id of -1 is padding.  Any other id outside [0, E) is treated as padding
+ * too and recorded in the workspace's error word; moe_build_row_map_check
+ * then returns MOE_ERR_INVALID_EXPERT.
+ * All arrays are device memory.  `workspace` is caller-owned device memory of
+ * at least moe_build_row_map_workspace_size(...) bytes, 16-byte aligned; it
+ * must not be shared by calls that may overlap on the GPU.
+ * Limits: 1 <= top_k <= MOE_MAX_TOP_K, 1 <= E <= MOE_MAX_EXPERTS,
+ * T * top_k < 2^31.  T == 0 writes counts = 0 and offsets = 0.
+ * ---------------------------------------------------------------------- */
+moe_status moe_build_row_map_workspace_size(int64_t T, int32_t top_k, int32_t E,
+                                            size_t *bytes);
+
+moe_status moe_build_row_map(const int32_t *topk_ids, int64_t T, int32_t top_k, int32_t E,
+                             int32_t *counts, int32_t *offsets, int32_t *row_map,
+                             int32_t *src_row, void *workspace, size_t workspace_bytes,
+                             moe_stream_t stream);
+
+/* Synchronises `stream`, then reads the error word that the last
+ * moe_build_row_map on `workspace` left there: MOE_OK or
+ * MOE_ERR_INVALID_EXPERT (or MOE_ERR_CUDA if the read fails). */
+moe_status moe_build_row_map_check(const void *workspace, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Combine + residual + RMSNorm + quantisation, one call.
+ * ---------------------------------------------------------------------- */
+typedef struct moe_combine_args {
+    int64_t T;                    /* tokens (rows of every [T, *] tensor); 0 = no-op */
+    int32_t H;                    /* hidden size; multiple of 8, <= MOE_MAX_HIDDEN */
+    int32_t top_k;                /* slots per token, 1..MOE_MAX_TOP_K */
+    const void *expert_out;       /* device bf16 [n_expert_rows, H], grouped by expert */
+    int64_t n_expert_rows;        /* rows in expert_out (row_map entries must be below) */
+    const int32_t *row_map;       /* device int32 [T, top_k], -1 = padded slot */
+    const float *router_weights;  /* device fp32 [T, top_k], used as given */
+    const void *shared_out;       /* device bf16 [T, H] or NULL: shared-expert row, weight 1 */
+    const void *residual;         /* device bf16 [T, H] or NULL */
+    const void *gamma;            /* device bf16 [H] or NULL = no RMSNorm */
+    float eps;                    /* RMSNorm epsilon, >= 0, inside the square root */
+    float weight_bias;            /* added to gamma: 0 standard, 1 Gemma form */
+    int32_t quant;                /* moe_quant_kind */
+    int32_t sf_layout;            /* moe_sf_layout (ignored when quant == NONE) */
+    float global_scale;           /* NVFP4 g > 0: codes encode g * y (ignored otherwise) */
+    int32_t reserved0;            /* must be 0 */
+    void *combined_out;           /* device bf16 [T, H] or NULL: bf16(s) */
+    void *residual_out;           /* device bf16 [T, H] or NULL: bf16(x) */
+    void *norm_out;               /* device bf16 [T, H] or NULL: bf16(y); needs gamma */
+    void *quant_out;              /* device uint8: [T, H] MXFP8 / [T, H/2] NVFP4; needs quant */
+    void *scales_out;             /* device uint8, moe_scales_bytes(...) bytes; needs quant */
+    int32_t *status;              /* device int32 or NULL: set to a nonzero moe_status
+                                     if the kernel meets a row_map entry >= n_expert_rows
+                                     (that slot is skipped) or a bounded wait gives up;
+                                     the caller zeroes it beforehand */
+} moe_combine_args;
+
+/* Enqueues the combine on `stream`.
+ * x is the unrounded fp32 sum; residual_out = bf16(x); the RMSNorm and the
+ * quantiser read the unrounded x (or y), not a bf16 copy.  Without gamma
+ * the quantiser reads x directly.  Without residual, x = s.
+ * Padded tokens (all slots -1) are still written: s = shared (or 0).
+ * Host-side validation, before any launch:
+ *   args non-NULL; T >= 0; H % 8 == 0 and 8 <= H <= MOE_MAX_HIDDEN;
+ *   1 <= top_k <= MOE_MAX_TOP_K; row_map, router_weights non-NULL;
+ *   expert_out non-NULL when n_expert_rows > 0; every bf16 / byte tensor
+ *   pointer 16-byte aligned; at least one output requested;
+ *   norm_out needs gamma; quant in {NONE, MXFP8, NVFP4}; MXFP8 needs
+ *   H % 32 == 0, NVFP4 needs H % 16 == 0 and a finite global_scale > 0;
+ *   quant needs quant_out and scales_out; sf_layout in {LINEAR, SWIZZLED}.
+ * Returns MOE_OK (enqueued), MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED or
+ * MOE_ERR_CUDA. */
+moe_status moe_combine(const moe_combine_args *args, moe_stream_t stream);
+
+/* Bytes of the scale matrix for T rows of H elements: linear T * C, swizzled
+ * roundup(T, 128) * roundup(C, 4), with C = H / 32 (MXFP8) or H / 16 (NVFP4). */
+moe_status moe_scales_bytes(int64_t T, int32_t H, int32_t quant, int32_t sf_layout,
+                            size_t *bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_COMBINE_H */

@@ -1,0 +1,607 @@
+// combine.cu -- the MoE combine/finalize kernel and its C entry point.
+//
+// What it computes (Struct_ep_combine_skip_a2a, execute: weighted sum of
+// routed expert outputs; fused_shared_expert; flashinfer.comm.
+// trtllm_moe_allreduce_fusion: residual_in/out, rms_gamma, rms_eps,
+// weight_bias, norm_out, quant_out, scale_out, layout_code;
+// flashinfer.comm.moe_a2a_combine: output_dtype float8_e4m3fn with UE8M0
+// output_scales per 32, output_scalar_scale for NVFP4, sf_layout):
+//
+//   s = sum_j w[t,j] * expert_out[row_map[t,j]]  (fp32, ascending j) + shared[t]
+//   x = s + residual[t]
+//   y = x / sqrt(mean(x^2) + eps) * (gamma + weight_bias)
+//   MXFP8: per 32 elements, e = smallest integer with amax <= 448 * 2^e,
+//          byte = clamp(e + 127, 0, 254), code = e4m3_rn_sat(y * 2^-e)
+//   NVFP4: v = g * y; per 16 elements s = e4m3_rn_sat(amax(v) / 6),
+//          code = e2m1_rn_sat(v / s) (0 when s == 0)
+//
+// Design (an HBM-bound gather; no tensor cores -- nothing here is a
+// contraction):
+//   * persistent CTAs, one per SM; token t goes to CTA t mod gridDim;
+//   * one producer warp walks the CTA's tokens and, for each row the token
+//     needs (its valid expert rows in ascending j, then the shared row, then
+//     the residual row), issues ONE cp.async.bulk of the whole 2H-byte row
+//     into the next slot of a ring of `stages` shared-memory row buffers,
+//     completing on that slot's "full" mbarrier; row_map / weights of the
+//     next token are prefetched while the current one is issued;
+//   * consumer warps own 8-element vectors v = slot * NC + thread of the row
+//     and accumulate fp32 in registers straight from the ring, then release
+//     the slot on its "empty" mbarrier;
+//   * after a token's last row: bf16 stores, a sum of squares reduced by warp
+//     shuffles and an mbarrier-synchronised cross-warp sum, the norm, and the
+//     block quantiser (an MXFP8 block is 4 consecutive lanes, NVFP4 2).
+// Every wait is bounded (kWaitLimitNs); a wait that gives up records
+// MOE_ERR_DEVICE_TIMEOUT and the CTA drains its own copies and returns.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.h"
+#include "ptx.cuh"
+
+namespace nqg {
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kMaxConsumerWarps = 8;  // with VPT <= 8 this covers H <= 16384
+constexpr int kMaxStages = 32;
+constexpr size_t kSmemBudget = 200 * 1024;
+
+enum : int32_t { F_EXPERT = 1, F_SHARED = 2, F_RESIDUAL = 4, F_LAST = 8, F_EMPTY = 16 };
+
+struct StageMeta {
+    int32_t t;
+    float w;
+    int32_t flags;
+    int32_t pad;
+};
+
+struct Params {
+    int64_t T;
+    int32_t H, k;
+    const uint8_t *expert_out;
+    int64_t n_rows;
+    const int32_t *row_map;
+    const float *weights;
+    const uint8_t *shared;
+    const uint8_t *residual;
+    const uint16_t *gamma;
+    float eps, wb, gscale;
+    int32_t sf_layout;
+    uint16_t *combined_out, *residual_out, *norm_out;
+    uint8_t *quant_out, *scales_out;
+    int32_t *status;
+    int32_t stages;
+    int64_t sf_cols, sf_cols_pad, sf_rows_pad;
+};
+
+struct SmemLayout {
+    uint32_t row_stride, bars, meta, red, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int32_t H, int32_t stages, int32_t ncw)
+{
+    SmemLayout L;
+    L.row_stride = (static_cast<uint32_t>(H) * 2u + 127u) & ~127u;
+    L.bars = static_cast<uint32_t>(stages) * L.row_stride;
+    L.meta = L.bars + (2u * stages + 2u) * 8u;  // full[S], empty[S], reduction barrier, pad
+    L.red = L.meta + static_cast<uint32_t>(stages) * static_cast<uint32_t>(sizeof(StageMeta));
+    L.total = L.red + 2u * static_cast<uint32_t>(ncw) * 4u;
+    return L;
+}
+
+__device__ __forceinline__ void report(int32_t *status, int32_t code)
+{
+    if (status)
+        atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t c, const Params &p)
+{
+    if (p.sf_layout == MOE_SF_LINEAR)
+        return r * p.sf_cols + c;
+    return (r >> 7) * (p.sf_cols_pad >> 2) * 512 + (c >> 2) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (c & 3);
+}
+
+__device__ __forceinline__ void store_bf16x8(uint16_t *base, int64_t off, const float *v)
+{
+    uint4 q;
+    q.x = f32x2_to_bf16x2(v[0], v[1]);
+    q.y = f32x2_to_bf16x2(v[2], v[3]);
+    q.z = f32x2_to_bf16x2(v[4], v[5]);
+    q.w = f32x2_to_bf16x2(v[6], v[7]);
+    *reinterpret_cast<uint4 *>(base + off) = q;
+}
+
+// UE8M0 byte of a block whose absolute maximum is `amax` (>= 0, finite):
+// the smallest e with amax <= 448 * 2^e -- with amax = m * 2^p, m in [1, 2),
+// that is e = p - 8 when m <= 1.75 and p - 7 otherwise -- biased by 127 and
+// clamped to [0, 254].
+__device__ __forceinline__ int32_t ue8m0_byte(float amax)
+{
+    const uint32_t bits = __float_as_uint(amax);
+    const int32_t ef = static_cast<int32_t>(bits >> 23);
+    if (ef == 0)
+        return 0;  // zero or below 2^-126: e <= -134 clamps to 0
+    const int32_t p = ef - 127;
+    const int32_t e = ((bits & 0x7FFFFFu) <= 0x600000u) ? p - 8 : p - 7;
+    const int32_t b = e + 127;
+    return b < 0 ? 0 : (b > 254 ? 254 : b);
+}
+
+template <int VPT, int QUANT>
+__global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) combine_kernel(const Params p)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ncw = (blockDim.x >> 5) - 1;
+    const int NC = ncw * 32;
+    const int S = p.stages;
+    const int32_t H = p.H, k = p.k;
+    const int32_t nvec = H >> 3;
+    const uint32_t row_bytes = static_cast<uint32_t>(H) * 2u;
+    const SmemLayout L = smem_layout(H, S, ncw);
+    const uint32_t ring = smem_u32(smem);
+    const uint32_t full0 = ring + L.bars, empty0 = full0 + 8u * S, redbar = empty0 + 8u * S;
+    StageMeta *meta = reinterpret_cast<StageMeta *>(smem + L.meta);
+    float *red = reinterpret_cast<float *>(smem + L.red);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, ncw);
+        }
+        mbar_init(redbar, ncw);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == ncw) {
+        // ------------------------------------------------------- producer
+        int stage = 0;
+        uint32_t phase = 0;
+        int64_t issued = 0;
+        bool ok = true;
+        int64_t t = blockIdx.x;
+        int32_t r_next = -1;
+        float w_next = 0.f;
+        if (t < p.T && lane < k) {
+            r_next = __ldg(p.row_map + t * k + lane);
+            w_next = __ldg(p.weights + t * k + lane);
+        }
+        for (; t < p.T && ok; t += gridDim.x) {
+            const int32_t r = r_next;
+            const float w = w_next;
+            const int64_t tn = t + gridDim.x;
+            if (tn < p.T && lane < k) {
+                r_next = __ldg(p.row_map + tn * k + lane);
+                w_next = __ldg(p.weights + tn * k + lane);
+            }
+            bool valid = lane < k && r >= 0;
+            if (valid && r >= p.n_rows) {
+                report(p.status, MOE_ERR_ROW_OUT_OF_RANGE);
+                valid = false;
+            }
+            uint32_t m = __ballot_sync(0xffffffffu, valid);
+            const int n_items = __popc(m) + (p.shared ? 1 : 0) + (p.residual ? 1 : 0);
+            int item = 0;
+            // lane 0 fills the next ring slot with one row (src == nullptr: an
+            // empty marker); false if the slot never freed up
+            auto produce = [&](const uint8_t *src, float wt, int32_t flags) {
+                bool good = true;
+                if (lane == 0) {
+                    good = mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, kWaitLimitNs);
+                    if (good) {
+                        meta[stage] = StageMeta{static_cast<int32_t>(t), wt, flags, 0};
+                        if (src) {
+                            mbar_arrive_expect_tx(full0 + 8u * stage, row_bytes);
+                            bulk_g2s(ring + static_cast<uint32_t>(stage) * L.row_stride, src, row_bytes,
+                                     full0 + 8u * stage);
+                        } else {
+                            mbar_arrive(full0 + 8u * stage);
+                        }
+                    }
+                }
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (good) {
+                    ++issued;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                return good;
+            };
+            if (n_items == 0) {
+                ok = produce(nullptr, 0.f, F_EMPTY | F_LAST);
+                continue;
+            }
+            while (m && ok) {
+                const int j = __ffs(m) - 1;
+                m &= m - 1;
+                const int32_t rj = __shfl_sync(0xffffffffu, r, j);
+                const float wj = __shfl_sync(0xffffffffu, w, j);
+                ++item;
+                ok = produce(p.expert_out + static_cast<int64_t>(rj) * row_bytes, wj,
+                             F_EXPERT | (item == n_items ? F_LAST : 0));
+            }
+            if (p.shared && ok) {
+                ++item;
+                ok = produce(p.shared + t * row_bytes, 1.f, F_SHARED | (item == n_items ? F_LAST : 0));
+            }
+            if (p.residual && ok) {
+                ++item;
+                ok = produce(p.residual + t * row_bytes, 1.f, F_RESIDUAL | F_LAST);
+            }
+        }
+        if (!ok && lane == 0) {
+            // a slot never freed up: record it, then let every copy this warp
+            // started land before the CTA's shared memory goes away
+            report(p.status, MOE_ERR_DEVICE_TIMEOUT);
+            const int64_t n = issued < S ? issued : S;
+            for (int64_t s = 0; s < n; ++s) {
+                const int64_t times = (issued - 1 - s) / S + 1;
+                mbar_wait_bounded(full0 + 8u * static_cast<uint32_t>(s), static_cast<uint32_t>((times - 1) & 1),
+                                  kWaitLimitNs);
+            }
+        }
+        return;
+    }
+
+    // ----------------------------------------------------------- consumers
+    const int tid = threadIdx.x;
+    // pad rows of a swizzled scale matrix are written as zero
+    if (QUANT != MOE_QUANT_NONE && p.sf_layout == MOE_SF_SWIZZLED_128x4 && p.sf_rows_pad > p.T) {
+        const int64_t n = (p.sf_rows_pad - p.T) * p.sf_cols_pad;
+        for (int64_t i = static_cast<int64_t>(blockIdx.x) * NC + tid; i < n;
+             i += static_cast<int64_t>(gridDim.x) * NC)
+            p.scales_out[sf_offset(p.T + i / p.sf_cols_pad, i % p.sf_cols_pad, p)] = 0;
+    }
+
+    const bool do_norm = p.gamma != nullptr;
+
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t tok = 0;
+    for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, ++tok) {
+        float acc[VPT][8];
+#pragma unroll
+        for (int s = 0; s < VPT; ++s)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                acc[s][i] = 0.f;
+        bool combined_done = false;
+        for (int it = 0; it < k + 3; ++it) {
+            if (!mbar_wait_bounded(full0 + 8u * stage, phase, kWaitLimitNs)) {
+                report(p.status, MOE_ERR_DEVICE_TIMEOUT);
+                return;
+            }
+            const StageMeta m = meta[stage];
+            if (!(m.flags & F_EMPTY)) {
+                if ((m.flags & F_RESIDUAL) && p.combined_out) {
+#pragma unroll
+                    for (int s = 0; s < VPT; ++s) {
+                        const int v = s * NC + tid;
+                        if (v < nvec)
+                            store_bf16x8(p.combined_out, t * H + 8 * v, acc[s]);
+                    }
+                    combined_done = true;
+                }
+                const uint8_t *row = smem + static_cast<uint32_t>(stage) * L.row_stride;
+                uint4 q[VPT];
+#pragma unroll
+                for (int s = 0; s < VPT; ++s) {
+                    const int v = s * NC + tid;
+                    if (v < nvec)
+                        q[s] = *reinterpret_cast<const uint4 *>(row + 16 * v);
+                }
+#pragma unroll
+                for (int s = 0; s < VPT; ++s) {
+                    const int v = s * NC + tid;
+                    if (v < nvec) {
+                        const uint32_t qw[4] = {q[s].x, q[s].y, q[s].z, q[s].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            float lo, hi;
+                            bf16x2_to_f32(qw[i], lo, hi);
+                            acc[s][2 * i] = fmaf(m.w, lo, acc[s][2 * i]);
+                            acc[s][2 * i + 1] = fmaf(m.w, hi, acc[s][2 * i + 1]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(empty0 + 8u * stage);
+            if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            if (m.flags & F_LAST)
+                break;
+        }
+
+        // ------------------------------------------------------ epilogue
+        const int64_t row0 = t * H;
+        if (p.combined_out && !combined_done) {
+#pragma unroll
+            for (int s = 0; s < VPT; ++s) {
+                const int v = s * NC + tid;
+                if (v < nvec)
+                    store_bf16x8(p.combined_out, row0 + 8 * v, acc[s]);
+            }
+        }
+        if (p.residual_out) {
+#pragma unroll
+            for (int s = 0; s < VPT; ++s) {
+                const int v = s * NC + tid;
+                if (v < nvec)
+                    store_bf16x8(p.residual_out, row0 + 8 * v, acc[s]);
+            }
+        }
+        if (do_norm) {
+            // gamma is re-read per token; it stays in L1 / L2
+            uint4 gq[VPT];
+#pragma unroll
+            for (int s = 0; s < VPT; ++s) {
+                const int v = s * NC + tid;
+                gq[s] = (v < nvec) ? __ldg(reinterpret_cast<const uint4 *>(p.gamma) + v) : make_uint4(0, 0, 0, 0);
+            }
+            float ss = 0.f;
+#pragma unroll
+            for (int s = 0; s < VPT; ++s)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    ss = fmaf(acc[s][i], acc[s][i], ss);  // vectors past H hold 0
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1)
+                ss += __shfl_xor_sync(0xffffffffu, ss, d);
+            float *part = red + (tok & 1u) * ncw;
+            if (lane == 0) {
+                part[warp] = ss;
+                mbar_arrive(redbar);
+            }
+            if (!mbar_wait_bounded(redbar, tok & 1u, kWaitLimitNs)) {
+                report(p.status, MOE_ERR_DEVICE_TIMEOUT);
+                return;
+            }
+            float total = 0.f;
+            for (int w = 0; w < ncw; ++w)
+                total += part[w];
+            const float rinv = 1.0f / sqrtf(total / static_cast<float>(H) + p.eps);
+#pragma unroll
+            for (int s = 0; s < VPT; ++s) {
+                const uint32_t gv[4] = {gq[s].x, gq[s].y, gq[s].z, gq[s].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float lo, hi;
+                    bf16x2_to_f32(gv[i], lo, hi);
+                    acc[s][2 * i] = acc[s][2 * i] * rinv * (lo + p.wb);
+                    acc[s][2 * i + 1] = acc[s][2 * i + 1] * rinv * (hi + p.wb);
+                }
+            }
+            if (p.norm_out) {
+#pragma unroll
+                for (int s = 0; s < VPT; ++s) {
+                    const int v = s * NC + tid;
+                    if (v < nvec)
+                        store_bf16x8(p.norm_out, row0 + 8 * v, acc[s]);
+                }
+            }
+        }
+
+        if constexpr (QUANT == MOE_QUANT_MXFP8) {
+#pragma unroll
+            for (int s = 0; s < VPT; ++s) {
+                const int v = s * NC + tid;
+                const bool vv = v < nvec;
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    amax = fmaxf(amax, fabsf(acc[s][i]));
+                amax = vv ? amax : 0.f;
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                const int32_t byte = ue8m0_byte(amax);
+                const float scale = __uint_as_float(static_cast<uint32_t>(254 - byte) << 23);  // 2^-e
+                if (vv) {
+                    uint2 qv;
+                    qv.x = cvt_e4m3x4(acc[s][0] * scale, acc[s][1] * scale, acc[s][2] * scale, acc[s][3] * scale);
+                    qv.y = cvt_e4m3x4(acc[s][4] * scale, acc[s][5] * scale, acc[s][6] * scale, acc[s][7] * scale);
+                    *reinterpret_cast<uint2 *>(p.quant_out + row0 + 8 * v) = qv;
+                    if ((lane & 3) == 0) {
+                        const int64_t c = v >> 2;
+                        p.scales_out[sf_offset(t, c, p)] = static_cast<uint8_t>(byte);
+                        if (c == p.sf_cols - 1)
+                            for (int64_t cp = p.sf_cols; cp < p.sf_cols_pad; ++cp)
+                                p.scales_out[sf_offset(t, cp, p)] = 0;
+                    }
+                }
+            }
+        } else if constexpr (QUANT == MOE_QUANT_NVFP4) {
+#pragma unroll
+            for (int s = 0; s < VPT; ++s) {
+                const int v = s * NC + tid;
+                const bool vv = v < nvec;
+                float g[8];
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    g[i] = acc[s][i] * p.gscale;
+                    amax = fmaxf(amax, fabsf(g[i]));
+                }
+                amax = vv ? amax : 0.f;
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                const uint32_t sc = cvt_e4m3x2(__fdiv_rn(amax, 6.0f), 0.f) & 0xFFu;
+                const float sf = e4m3_code_value(sc);
+                if (vv) {
+                    uint32_t packed = 0;
+                    if (sf != 0.f) {
+                        float qv[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            qv[i] = __fdiv_rn(g[i], sf);
+                        packed = cvt_e2m1x8(qv);
+                    }
+                    *reinterpret_cast<uint32_t *>(p.quant_out + (row0 >> 1) + 4 * v) = packed;
+                    if ((lane & 1) == 0) {
+                        const int64_t c = v >> 1;
+                        p.scales_out[sf_offset(t, c, p)] = static_cast<uint8_t>(sc);
+                        if (c == p.sf_cols - 1)
+                            for (int64_t cp = p.sf_cols; cp < p.sf_cols_pad; ++cp)
+                                p.scales_out[sf_offset(t, cp, p)] = 0;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------- host
+
+struct Plan {
+    int vpt, ncw, stages;
+    SmemLayout smem;
+};
+
+// Vectors per consumer thread: the smallest of 1, 2, 4, 8 that covers the
+// row with at most kMaxConsumerWarps consumer warps; ring depth: as many
+// whole rows as fit the shared-memory budget, 2..32.
+Plan make_plan(int32_t H)
+{
+    Plan pl{};
+    const int nvec = H / 8;
+    pl.vpt = 8;
+    for (int v : {1, 2, 4, 8}) {
+        if ((nvec + 32 * v - 1) / (32 * v) <= kMaxConsumerWarps) {
+            pl.vpt = v;
+            break;
+        }
+    }
+    pl.ncw = (nvec + 32 * pl.vpt - 1) / (32 * pl.vpt);
+    const SmemLayout one = smem_layout(H, 1, pl.ncw);
+    const size_t fixed = one.total - one.row_stride - 16 - sizeof(StageMeta);
+    const size_t per_stage = one.row_stride + 16 + sizeof(StageMeta);
+    const int s = static_cast<int>((kSmemBudget - fixed) / per_stage);
+    pl.stages = s < 2 ? 2 : (s > kMaxStages ? kMaxStages : s);
+    pl.smem = smem_layout(H, pl.stages, pl.ncw);
+    return pl;
+}
+
+template <int VPT, int QUANT>
+moe_status launch_t(const Params &p, const Plan &pl, cudaStream_t stream)
+{
+    auto kern = combine_kernel<VPT, QUANT>;
+    static int configured_for[64] = {0};  // per device: dynamic smem already allowed
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const int need = static_cast<int>(pl.smem.total);
+    if (dev < 0 || dev >= 64 || configured_for[dev] < need) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, need) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (dev >= 0 && dev < 64)
+            configured_for[dev] = need;
+    }
+    const int64_t ctas = sm_count();
+    if (ctas <= 0)
+        return MOE_ERR_CUDA;
+    const int grid = static_cast<int>(p.T < ctas ? p.T : ctas);
+    kern<<<grid, (pl.ncw + 1) * 32, pl.smem.total, stream>>>(p);
+    return launch_status();
+}
+
+template <int QUANT>
+moe_status launch_q(const Params &p, const Plan &pl, cudaStream_t stream)
+{
+    switch (pl.vpt) {
+    case 1: return launch_t<1, QUANT>(p, pl, stream);
+    case 2: return launch_t<2, QUANT>(p, pl, stream);
+    case 4: return launch_t<4, QUANT>(p, pl, stream);
+    default: return launch_t<8, QUANT>(p, pl, stream);
+    }
+}
+
+} // namespace
+} // namespace nqg
+
+using namespace nqg;
+
+extern "C" moe_status moe_combine(const moe_combine_args *a, moe_stream_t stream)
+{
+    if (!a)
+        return MOE_ERR_INVALID_ARG;
+    if (a->T < 0 || a->reserved0 != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (a->H < 8 || a->H % 8 != 0 || a->top_k < 1)
+        return MOE_ERR_INVALID_ARG;
+    if (a->H > MOE_MAX_HIDDEN || a->top_k > MOE_MAX_TOP_K)
+        return MOE_ERR_UNSUPPORTED;
+    if (!a->row_map || !a->router_weights || a->n_expert_rows < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (a->n_expert_rows > 0 && !a->expert_out)
+        return MOE_ERR_INVALID_ARG;
+    if (a->quant != MOE_QUANT_NONE && a->quant != MOE_QUANT_MXFP8 && a->quant != MOE_QUANT_NVFP4)
+        return MOE_ERR_INVALID_ARG;
+    if (a->quant != MOE_QUANT_NONE) {
+        if (a->sf_layout != MOE_SF_LINEAR && a->sf_layout != MOE_SF_SWIZZLED_128x4)
+            return MOE_ERR_INVALID_ARG;
+        if (!a->quant_out || !a->scales_out)
+            return MOE_ERR_INVALID_ARG;
+        if (a->quant == MOE_QUANT_MXFP8 && a->H % 32 != 0)
+            return MOE_ERR_INVALID_ARG;
+        if (a->quant == MOE_QUANT_NVFP4 &&
+            (a->H % 16 != 0 || !(a->global_scale > 0.f) || !(a->global_scale < 3.0e38f)))
+            return MOE_ERR_INVALID_ARG;
+    }
+    if (a->norm_out && !a->gamma)
+        return MOE_ERR_INVALID_ARG;
+    if (!(a->eps >= 0.f) || !(a->eps < 3.0e38f) || !(a->weight_bias == a->weight_bias))
+        return MOE_ERR_INVALID_ARG;
+    if (!a->combined_out && !a->residual_out && !a->norm_out && a->quant == MOE_QUANT_NONE)
+        return MOE_ERR_INVALID_ARG;
+    const void *must16[] = {a->expert_out, a->shared_out, a->residual, a->gamma, a->combined_out,
+                            a->residual_out, a->norm_out, a->quant_out};
+    for (const void *q : must16)
+        if (q && !aligned16(q))
+            return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(a->row_map) & 3u) || (reinterpret_cast<uintptr_t>(a->router_weights) & 3u) ||
+        (reinterpret_cast<uintptr_t>(a->status) & 3u))
+        return MOE_ERR_INVALID_ARG;
+    if (a->T == 0)
+        return MOE_OK;
+
+    Params p{};
+    p.T = a->T;
+    p.H = a->H;
+    p.k = a->top_k;
+    p.expert_out = static_cast<const uint8_t *>(a->expert_out);
+    p.n_rows = a->n_expert_rows;
+    p.row_map = a->row_map;
+    p.weights = a->router_weights;
+    p.shared = static_cast<const uint8_t *>(a->shared_out);
+    p.residual = static_cast<const uint8_t *>(a->residual);
+    p.gamma = static_cast<const uint16_t *>(a->gamma);
+    p.eps = a->eps;
+    p.wb = a->weight_bias;
+    p.gscale = a->global_scale;
+    p.sf_layout = a->sf_layout;
+    p.combined_out = static_cast<uint16_t *>(a->combined_out);
+    p.residual_out = static_cast<uint16_t *>(a->residual_out);
+    p.norm_out = static_cast<uint16_t *>(a->norm_out);
+    p.quant_out = static_cast<uint8_t *>(a->quant_out);
+    p.scales_out = static_cast<uint8_t *>(a->scales_out);
+    p.status = a->status;
+    if (a->quant != MOE_QUANT_NONE) {
+        p.sf_cols = a->H / (a->quant == MOE_QUANT_MXFP8 ? 32 : 16);
+        p.sf_cols_pad = a->sf_layout == MOE_SF_LINEAR ? p.sf_cols : (p.sf_cols + 3) / 4 * 4;
+        p.sf_rows_pad = a->sf_layout == MOE_SF_LINEAR ? p.T : (p.T + 127) / 128 * 128;
+    }
+    const Plan pl = make_plan(a->H);
+    p.stages = pl.stages;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    switch (a->quant) {
+    case MOE_QUANT_MXFP8: return launch_q<MOE_QUANT_MXFP8>(p, pl, s);
+    case MOE_QUANT_NVFP4: return launch_q<MOE_QUANT_NVFP4>(p, pl, s);
+    default: return launch_q<MOE_QUANT_NONE>(p, pl, s);
+    }
+}

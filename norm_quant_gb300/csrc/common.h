@@ -1,0 +1,23 @@
+// common.h -- host-side helpers shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moe_combine.h"
+
+namespace nqg {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count();
+
+// Status of the launches just made: MOE_ERR_CUDA if any failed.
+inline moe_status launch_status()
+{
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+} // namespace nqg

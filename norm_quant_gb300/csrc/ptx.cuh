@@ -1,0 +1,146 @@
+// ptx.cuh -- thin inline-PTX wrappers used by the sm_103a kernels:
+// mbarrier, 1-D bulk async copies (TMA engine), the global timer, and the
+// hardware fp8 / fp4 / bf16 conversions.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nqg {
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Makes the initialised barriers visible to the async proxy (bulk copies).
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{ .reg .pred p;\n"
+                 "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                 "  selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase of parity `parity` to complete, for at most
+// `limit_ns` of wall-clock time.  Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (globaltimer_ns() - t0 > limit_ns)
+            return false;
+    }
+}
+
+// ---------------------------------------------------------- bulk copies
+
+// One contiguous global -> shared copy through the TMA engine; completion is
+// signalled on `bar` as `bytes` transaction bytes.  src, dst and bytes must
+// be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// ------------------------------------------------------------ conversions
+
+// Two fp32 -> two e4m3 (round to nearest even, saturate to +-448); `lo`
+// lands in the low byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Four fp32 -> four e4m3 bytes, element 0 in the lowest byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float d)
+{
+    return cvt_e4m3x2(a, b) | (cvt_e4m3x2(c, d) << 16);
+}
+
+// Eight fp32 -> eight e2m1 nibbles (round to nearest even, saturate to +-6),
+// element 0 in the lowest nibble.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float *v)
+{
+    uint32_t r;
+    asm("{ .reg .b8 b0, b1, b2, b3;\n"
+        "  cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+        "  cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+        "  cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+        "  cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+        "  mov.b32 %0, {b0, b1, b2, b3}; }"
+        : "=r"(r)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return r;
+}
+
+// Value of a non-negative e4m3 code (s.eeee.mmm, bias 7, subnormals at
+// exponent field 0), built from the format's definition.
+__device__ __forceinline__ float e4m3_code_value(uint32_t c)
+{
+    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+    if (e == 0)
+        return static_cast<float>(m) * 0x1p-9f;
+    return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// bf16x2 (as a 32-bit word) -> two fp32, exact.
+__device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float &lo, float &hi)
+{
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xFFFF0000u);
+}
+
+// Two fp32 -> bf16x2, round to nearest even; `lo` in the low half.
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+} // namespace nqg

@@ -1,0 +1,301 @@
+// route.cu -- routing build: per-expert histogram, exclusive scan and stable
+// scatter to row_map (Struct_ep_combine_skip_a2a: topk_ids, src_info,
+// recv_count_ptrs; flashinfer.megamoe.nvfp4_mega_moe: num_tokens padding
+// with -1 and cumulative_local_expert_recv_stats).
+//
+// The N = T * top_k slots are cut into chunks of kChunk consecutive slots,
+// one warp per chunk:
+//   K1 route_hist     hist[c][e] = slots of chunk c routed to e
+//   K2 route_scan     counts[e] = sum_c hist[c][e]; offsets = exclusive scan
+//                     of counts; base[c][e] = offsets[e] + sum_{c'<c} hist[c'][e]
+//                     (written over hist)
+//   K3 route_scatter  row_map[i] = base[c][e] + rank of slot i among the slots
+//                     of chunk c before it with the same expert
+// Ranks come from __match_any_sync over 32 slots at a time plus a running
+// per-expert count in shared memory, so the result is deterministic and
+// bit-exact: no atomics decide a position.  No kernel waits on another CTA.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.h"
+
+namespace nqg {
+namespace {
+
+constexpr int kChunk = 1024;           // slots per warp-chunk
+constexpr int kPerLane = kChunk / 32;  // slots per lane per chunk
+constexpr int kScanMaxGroups = 32;     // route_scan uses up to 32 warps
+constexpr size_t kScanSmemBudget = 200 * 1024;
+
+struct WorkspaceLayout {
+    int64_t chunks;
+    size_t hist_off, err_off, total;
+};
+
+WorkspaceLayout layout_for(int64_t N, int32_t E)
+{
+    WorkspaceLayout L;
+    L.chunks = (N + kChunk - 1) / kChunk;
+    L.err_off = 0;  // error word first, padded to 16 bytes
+    L.hist_off = 16;
+    L.total = L.hist_off + static_cast<size_t>(L.chunks) * static_cast<size_t>(E) * sizeof(int32_t);
+    L.total = (L.total + 255) / 256 * 256;
+    return L;
+}
+
+int warps_per_cta(int32_t E)
+{
+    int w = static_cast<int>((48 * 1024) / (static_cast<size_t>(E) * sizeof(int32_t)));
+    return w < 1 ? 1 : (w > 8 ? 8 : w);
+}
+
+__global__ void route_hist_kernel(const int32_t *__restrict__ ids, int64_t N, int32_t E,
+                                  int32_t *__restrict__ hist, int64_t chunks, int32_t *__restrict__ err)
+{
+    extern __shared__ int32_t sh[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp;
+    if (c >= chunks)
+        return;
+    int32_t *h = sh + static_cast<size_t>(warp) * E;
+    for (int e = lane; e < E; e += 32)
+        h[e] = 0;
+    __syncwarp();
+    const int64_t base = c * kChunk;
+    int32_t v[kPerLane];
+#pragma unroll
+    for (int it = 0; it < kPerLane; ++it) {
+        const int64_t i = base + it * 32 + lane;
+        v[it] = (i < N) ? __ldg(ids + i) : -1;
+    }
+    bool bad = false;
+#pragma unroll
+    for (int it = 0; it < kPerLane; ++it) {
+        const int32_t e = v[it];
+        if (e >= 0 && e < E)
+            atomicAdd(&h[e], 1);
+        else if (e != -1)
+            bad = true;
+    }
+    __syncwarp();
+    int32_t *out = hist + c * E;
+    for (int e = lane; e < E; e += 32)
+        out[e] = h[e];
+    if (__any_sync(0xffffffffu, bad) && lane == 0)
+        atomicOr(err, 1);
+}
+
+// Warps of route_scan: as many as fit the shared-memory budget, up to 32.
+int scan_groups(int32_t E)
+{
+    const size_t tiles = (static_cast<size_t>(E) + 31) / 32;
+    const size_t per_group = tiles * 32 * sizeof(int32_t);
+    const size_t g = (kScanSmemBudget - (static_cast<size_t>(E) + 1) * sizeof(int32_t)) / per_group;
+    return static_cast<int>(g < 1 ? 1 : (g > kScanMaxGroups ? kScanMaxGroups : g));
+}
+
+// One CTA of 32 * ngroups threads.  Thread (g, lane) with g = threadIdx.x / 32
+// owns, for every tile of 32 experts, expert tile*32 + lane over the chunk
+// range of group g.
+__global__ void __launch_bounds__(kScanMaxGroups * 32) route_scan_kernel(int32_t *__restrict__ hist,
+                                                                        int64_t chunks, int32_t E,
+                                                                        int32_t *__restrict__ counts,
+                                                                        int32_t *__restrict__ offsets)
+{
+    extern __shared__ int32_t sh[];
+    const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ngroups = blockDim.x >> 5;
+    const int tiles = (E + 31) / 32;
+    const int64_t per = (chunks + ngroups - 1) / ngroups;
+    const int64_t c0 = g * per, c1 = (c0 + per < chunks) ? c0 + per : chunks;
+    int32_t *part = sh;                                             // [tiles][ngroups][32]
+    int32_t *tot = sh + static_cast<size_t>(tiles) * ngroups * 32;  // [E + 1]
+
+    // 1. per-(group, expert) sums of the group's chunks
+    for (int tile = 0; tile < tiles; ++tile) {
+        const int e = tile * 32 + lane;
+        int32_t s = 0;
+        if (e < E) {
+#pragma unroll 8
+            for (int64_t c = c0; c < c1; ++c)
+                s += hist[c * E + e];
+        }
+        part[(tile * ngroups + g) * 32 + lane] = s;
+    }
+    __syncthreads();
+    // 2. exclusive scan over groups per expert; expert totals
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int tile = e >> 5, l = e & 31;
+        int32_t run = 0;
+        for (int gg = 0; gg < ngroups; ++gg) {
+            int32_t *p = &part[(tile * ngroups + gg) * 32 + l];
+            const int32_t v = *p;
+            *p = run;
+            run += v;
+        }
+        tot[e] = run;
+        counts[e] = run;
+    }
+    __syncthreads();
+    // 3. exclusive scan over experts: each lane of warp 0 takes a contiguous
+    //    range, then a warp scan of the range sums
+    if (threadIdx.x < 32) {
+        const int per_e = (E + 31) / 32;
+        const int e0 = lane * per_e, e1 = (e0 + per_e < E) ? e0 + per_e : E;
+        int32_t s = 0;
+        for (int e = e0; e < e1; ++e)
+            s += tot[e];
+        int32_t incl = s;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d)
+                incl += o;
+        }
+        int32_t run = incl - s;
+        for (int e = e0; e < e1; ++e) {
+            const int32_t v = tot[e];
+            tot[e] = run;
+            offsets[e] = run;
+            run += v;
+        }
+        if (lane == 31)
+            offsets[E] = incl;
+    }
+    __syncthreads();
+    // 4. base[c][e] = offsets[e] + group prefix + running sum inside the group
+    for (int tile = 0; tile < tiles; ++tile) {
+        const int e = tile * 32 + lane;
+        if (e >= E)
+            continue;
+        int32_t run = tot[e] + part[(tile * ngroups + g) * 32 + lane];
+        for (int64_t c = c0; c < c1; ++c) {
+            const int32_t v = hist[c * E + e];
+            hist[c * E + e] = run;
+            run += v;
+        }
+    }
+}
+
+__global__ void route_scatter_kernel(const int32_t *__restrict__ ids, int64_t N, int32_t E,
+                                     const int32_t *__restrict__ base, int64_t chunks,
+                                     int32_t *__restrict__ row_map, int32_t *__restrict__ src_row)
+{
+    extern __shared__ int32_t sh[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp;
+    if (c >= chunks)
+        return;
+    int32_t *run = sh + static_cast<size_t>(warp) * E;
+    const int32_t *b = base + c * E;
+    for (int e = lane; e < E; e += 32)
+        run[e] = b[e];
+    const int64_t first = c * kChunk;
+    int32_t v[kPerLane];
+#pragma unroll
+    for (int it = 0; it < kPerLane; ++it) {
+        const int64_t i = first + it * 32 + lane;
+        v[it] = (i < N) ? __ldg(ids + i) : -1;
+    }
+    __syncwarp();
+    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int it = 0; it < kPerLane; ++it) {
+        const int64_t i = first + it * 32 + lane;
+        const int32_t e = v[it];
+        const bool valid = (e >= 0) && (e < E);
+        const uint32_t peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+        const int rank = __popc(peers & lt);
+        if (valid) {
+            const int32_t r = run[e] + rank;
+            row_map[i] = r;
+            if (src_row)
+                src_row[r] = static_cast<int32_t>(i);
+        } else if (i < N) {
+            row_map[i] = -1;
+        }
+        __syncwarp();
+        if (valid && rank == 0)
+            run[e] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+} // namespace
+} // namespace nqg
+
+using namespace nqg;
+
+extern "C" moe_status moe_build_row_map_workspace_size(int64_t T, int32_t top_k, int32_t E, size_t *bytes)
+{
+    if (!bytes || T < 0 || top_k < 1 || E < 1)
+        return MOE_ERR_INVALID_ARG;
+    if (top_k > MOE_MAX_TOP_K || E > MOE_MAX_EXPERTS || T * top_k >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED;
+    *bytes = layout_for(T * top_k, E).total;
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_build_row_map(const int32_t *topk_ids, int64_t T, int32_t top_k, int32_t E,
+                                        int32_t *counts, int32_t *offsets, int32_t *row_map,
+                                        int32_t *src_row, void *workspace, size_t workspace_bytes,
+                                        moe_stream_t stream)
+{
+    if (T < 0 || top_k < 1 || E < 1 || !counts || !offsets)
+        return MOE_ERR_INVALID_ARG;
+    if (top_k > MOE_MAX_TOP_K || E > MOE_MAX_EXPERTS || T * top_k >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!topk_ids || !row_map))
+        return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(topk_ids) | reinterpret_cast<uintptr_t>(counts) |
+         reinterpret_cast<uintptr_t>(offsets) | reinterpret_cast<uintptr_t>(row_map) |
+         reinterpret_cast<uintptr_t>(src_row)) & 3u)
+        return MOE_ERR_INVALID_ARG;
+    const int64_t N = T * top_k;
+    const WorkspaceLayout L = layout_for(N, E);
+    if (!workspace)
+        return MOE_ERR_WORKSPACE;
+    if (!aligned16(workspace))
+        return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < L.total)
+        return MOE_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    int32_t *err = reinterpret_cast<int32_t *>(ws + L.err_off);
+    int32_t *hist = reinterpret_cast<int32_t *>(ws + L.hist_off);
+    if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (N == 0) {
+        if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s) != cudaSuccess ||
+            cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    const int wpc = warps_per_cta(E);
+    const int grid = static_cast<int>((L.chunks + wpc - 1) / wpc);
+    const size_t sh = static_cast<size_t>(wpc) * E * sizeof(int32_t);
+    route_hist_kernel<<<grid, wpc * 32, sh, s>>>(topk_ids, N, E, hist, L.chunks, err);
+    const int tiles = (E + 31) / 32;
+    const int groups = scan_groups(E);
+    const size_t sh_scan = (static_cast<size_t>(tiles) * groups * 32 + E + 1) * sizeof(int32_t);
+    if (sh_scan > 48 * 1024 &&
+        cudaFuncSetAttribute(route_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sh_scan)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    route_scan_kernel<<<1, groups * 32, sh_scan, s>>>(hist, L.chunks, E, counts, offsets);
+    route_scatter_kernel<<<grid, wpc * 32, sh, s>>>(topk_ids, N, E, hist, L.chunks, row_map, src_row);
+    return launch_status();
+}
+
+extern "C" moe_status moe_build_row_map_check(const void *workspace, moe_stream_t stream)
+{
+    if (!workspace)
+        return MOE_ERR_INVALID_ARG;
+    int32_t err = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&err, workspace, sizeof(err), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return err ? MOE_ERR_INVALID_EXPERT : MOE_OK;
+}

@@ -81,6 +81,8 @@ def lib() -> C.CDLL:
             L.oracle_ue8m0_for_amax.argtypes = [C.c_double]
             L.oracle_sf_offset.restype = C.c_int64
             L.oracle_sf_offset.argtypes = [C.c_int64, C.c_int64, C.c_int64, C.c_int32]
+            L.oracle_sf_offsets.restype = None
+            L.oracle_sf_offsets.argtypes = [C.c_int64, C.c_int64, C.c_int32, C.c_void_p]
             L.oracle_scales_bytes.restype = C.c_int64
             L.oracle_scales_bytes.argtypes = [C.c_int64, C.c_int32, C.c_int32, C.c_int32]
             L.oracle_build_row_map.restype = C.c_int
@@ -156,6 +158,13 @@ def ue8m0_for_amax(amax) -> np.ndarray:
 
 def sf_offset(r: int, c: int, C_cols: int, layout="linear") -> int:
     return int(lib().oracle_sf_offset(int(r), int(c), int(C_cols), LAYOUT[layout]))
+
+
+def sf_offsets(T: int, C_cols: int, layout="linear") -> np.ndarray:
+    """int64 [T, C_cols] table of sf_offset(r, c)."""
+    out = np.zeros((T, C_cols), np.int64)
+    lib().oracle_sf_offsets(int(T), int(C_cols), LAYOUT[layout], _ptr(out))
+    return out
 
 
 def scales_bytes(T: int, H: int, quant: str, layout="linear") -> int:

@@ -202,6 +202,14 @@ int64_t oracle_sf_offset(int64_t r, int64_t c, int64_t C, int32_t layout)
            ((r % 128) / 32) * 4 + (c % 4);
 }
 
+/* out[r * C + c] = oracle_sf_offset(r, c, C, layout) for r < T, c < C. */
+void oracle_sf_offsets(int64_t T, int64_t C, int32_t layout, int64_t *out)
+{
+    for (int64_t r = 0; r < T; r++)
+        for (int64_t c = 0; c < C; c++)
+            out[r * C + c] = oracle_sf_offset(r, c, C, layout);
+}
+
 /* Size in bytes of the scale matrix for T rows and H elements per row. */
 int64_t oracle_scales_bytes(int64_t T, int32_t H, int32_t quant, int32_t layout)
 {

@@ -1,0 +1,195 @@
+"""Shared machinery of the parity tests: run a workload through the C ABI on
+the GPU and through the oracle on the CPU, and compare with the stated
+tolerances.
+
+Tolerances (from the task's correctness bar, derived in the design doc):
+  * routing (counts, offsets, row_map, src_row): bit-exact;
+  * bf16 outputs: |gpu - oracle| <= 2 bf16 ulps of the oracle value plus
+    gamma_k * (sum of |terms|), gamma_k = (k + 3) * 2^-24 the fp32 forward
+    error bound of the (k + 2)-term sum, carried through the norm's scale;
+  * block scales: identical bytes except in at most 0.01 % of blocks, which
+    may differ by one step;
+  * dequantised values: within one quantisation step of the coarser of the
+    two block scales.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import norm_quant_gb300 as nqg
+import oracle
+
+DEV = "cuda"
+
+
+def d(a: np.ndarray) -> torch.Tensor:
+    """numpy -> CUDA tensor, byte-for-byte (uint16 bf16 bits travel as int16)."""
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def h(t: torch.Tensor, dtype=None) -> np.ndarray:
+    a = t.cpu().numpy()
+    if dtype is not None:
+        a = a.view(dtype)
+    return a
+
+
+def gpu_route(ids: np.ndarray, E: int, stream=None):
+    T, k = ids.shape
+    d_ids = d(ids.astype(np.int32))
+    counts = torch.full((E,), -7, dtype=torch.int32, device=DEV)
+    offsets = torch.full((E + 1,), -7, dtype=torch.int32, device=DEV)
+    row_map = torch.full((T, k), -7, dtype=torch.int32, device=DEV)
+    src_row = torch.full((max(T * k, 1),), -7, dtype=torch.int32, device=DEV)
+    ws = torch.zeros(nqg.moe_build_row_map_workspace_size(T, k, E), dtype=torch.uint8, device=DEV)
+    nqg.moe_build_row_map(d_ids, E, counts, offsets, row_map, src_row, ws, stream=stream)
+    st = nqg.moe_build_row_map_check(ws, stream=stream)
+    return st, counts, offsets, row_map, src_row
+
+
+def gpu_combine(wl, inp, d_row_map, *, global_scale=1.0, outputs=None, stream=None,
+                canary=False):
+    """Runs moe_combine for workload `wl` on device copies of `inp`.
+    Returns host numpy outputs (bf16 as uint16 bits) and the status word."""
+    T, H, k = wl.T, wl.H, wl.k
+    outputs = outputs or wl.outputs
+    ex = d(inp["expert_out"]) if inp["n_valid"] else torch.zeros((0, H), dtype=torch.int16, device=DEV)
+    w = d(inp["weights"])
+    sh = d(inp["shared"]) if inp["shared"] is not None else None
+    rs = d(inp["residual"]) if inp["residual"] is not None else None
+    gm = d(inp["gamma"]) if inp["gamma"] is not None else None
+    pad = 4096 if canary else 0
+
+    def out(n, dtype):
+        buf = torch.full((n + 2 * pad,), 0x5A if dtype == torch.uint8 else 0x5A5A, dtype=dtype,
+                         device=DEV)
+        return buf, buf[pad:pad + n]
+
+    bufs, views = {}, {}
+    for name in ("combined", "residual", "norm"):
+        if name in outputs:
+            bufs[name], views[name] = out(T * H, torch.int16)
+    if wl.quant and "quant" in outputs:
+        qn = T * H if wl.quant == "mxfp8" else T * H // 2
+        bufs["quant"], views["quant"] = out(qn, torch.uint8)
+        sn = nqg.moe_scales_bytes(T, H, wl.quant, wl.sf_layout)
+        bufs["scales"], views["scales"] = out(sn, torch.uint8)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    nqg.moe_combine(stream=stream, expert_out=ex, row_map=d_row_map, router_weights=w,
+                    shared_out=sh, residual=rs, gamma=gm, eps=wl.eps, weight_bias=wl.weight_bias,
+                    quant=wl.quant, sf_layout=wl.sf_layout, global_scale=global_scale,
+                    combined_out=views.get("combined"), residual_out=views.get("residual"),
+                    norm_out=views.get("norm"), quant_out=views.get("quant"),
+                    scales_out=views.get("scales"), status=status, H=H)
+    torch.cuda.synchronize()
+    res = {"status": int(status.item())}
+    for name, v in views.items():
+        res[name] = h(v, np.uint16 if v.dtype == torch.int16 else np.uint8)
+        if canary:
+            b = h(bufs[name], np.uint16 if v.dtype == torch.int16 else np.uint8)
+            fill = 0x5A5A if v.dtype == torch.int16 else 0x5A
+            assert np.all(b[:pad] == fill) and np.all(b[pad + v.numel():] == fill), f"{name} overrun"
+    for name in ("combined", "residual", "norm"):
+        if name in res:
+            res[name] = res[name].reshape(T, H)
+    if "quant" in res:
+        res["quant"] = res["quant"].reshape(T, -1)
+    return res
+
+
+def oracle_combine(wl, inp, row_map: np.ndarray, *, tokens=None, global_scale=1.0,
+                   sf_layout=None):
+    """Oracle outputs for all tokens, or for the listed token rows only
+    (then in linear scale layout, indexed by position in `tokens`)."""
+    sel = slice(None) if tokens is None else np.asarray(tokens)
+    pick = (lambda a: a) if tokens is None else (lambda a: None if a is None else a[sel])
+    return oracle.combine(
+        inp["expert_out"], row_map[sel], inp["weights"][sel], shared=pick(inp["shared"]),
+        residual=pick(inp["residual"]), gamma=inp["gamma"], eps=wl.eps,
+        weight_bias=wl.weight_bias, quant=wl.quant,
+        sf_layout=(sf_layout or (wl.sf_layout if tokens is None else "linear")),
+        global_scale=global_scale)
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    a = np.abs(x)
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def sum_magnitude(inp, row_map: np.ndarray, tokens) -> np.ndarray:
+    """Per element sum of |terms| of x = sum_j w x_j + shared + residual."""
+    tokens = np.asarray(tokens)
+    H = inp["expert_out"].shape[1] if inp["n_valid"] else (
+        inp["residual"].shape[1] if inp["residual"] is not None else 1)
+    mag = np.zeros((tokens.size, H))
+    rows = inp["expert_out"]
+    for i, t in enumerate(tokens):
+        for j in range(row_map.shape[1]):
+            r = row_map[t, j]
+            if r >= 0:
+                mag[i] += abs(float(inp["weights"][t, j])) * np.abs(oracle.bf16_to_f64(rows[r]))
+        if inp["shared"] is not None:
+            mag[i] += np.abs(oracle.bf16_to_f64(inp["shared"][t]))
+        if inp["residual"] is not None:
+            mag[i] += np.abs(oracle.bf16_to_f64(inp["residual"][t]))
+    return mag
+
+
+def assert_bf16_close(got: np.ndarray, want: np.ndarray, abs_floor, what: str):
+    g = oracle.bf16_to_f64(got)
+    w = oracle.bf16_to_f64(want)
+    tol = 2 * bf16_ulp(w) + abs_floor
+    bad = np.abs(g - w) > tol
+    if bad.any():
+        i = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} beyond tolerance; "
+                             f"first {[(tuple(x), g[tuple(x)], w[tuple(x)]) for x in i]}")
+
+
+def quant_step(codes_deq_scaled: np.ndarray, quant: str) -> np.ndarray:
+    """Spacing of the element grid at a scaled magnitude (e4m3 or e2m1)."""
+    a = np.abs(codes_deq_scaled)
+    if quant == "mxfp8":
+        e = np.floor(np.log2(np.maximum(a, 2.0 ** -6)))
+        return 2.0 ** (e - 3)          # subnormal spacing 2^-9 below 2^-6
+    return np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))
+
+
+def assert_quant_close(wl, got_q, got_s, want_q, want_s, T, H, global_scale, what,
+                       layout=None):
+    layout = layout or wl.sf_layout
+    vec = 32 if wl.quant == "mxfp8" else 16
+    Cc = H // vec
+    idx = oracle.sf_offsets(T, Cc, layout)
+    gs, ws = got_s[idx], want_s[idx]
+    diff = gs.astype(np.int64) - ws.astype(np.int64)
+    n_bad = int((diff != 0).sum())
+    assert n_bad <= int(1e-4 * diff.size), f"{what}: {n_bad} of {diff.size} scale bytes differ"
+    assert np.all(np.abs(diff) <= 1), f"{what}: a scale byte differs by more than one step"
+    dg = oracle.dequant(got_q, got_s, T, H, wl.quant, layout, global_scale)
+    dw = oracle.dequant(want_q, want_s, T, H, wl.quant, layout, global_scale)
+    if wl.quant == "mxfp8":
+        sc = 2.0 ** (np.maximum(gs, ws).astype(np.float64) - 127)
+    else:
+        sc = np.maximum(oracle.e4m3_to_f64(gs), oracle.e4m3_to_f64(ws)) / global_scale
+    sc = np.repeat(sc, vec, axis=1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        scaled = np.where(sc > 0, np.maximum(np.abs(dg), np.abs(dw)) / sc, 0.0)
+    step = quant_step(scaled, wl.quant) * sc
+    bad = np.abs(dg - dw) > step
+    assert not bad.any(), f"{what}: {int(bad.sum())} dequantised values beyond one step"
+    same = (got_q == want_q).mean()
+    assert same >= 0.999, f"{what}: only {same:.5f} of code bytes identical"
+
+
+def nvfp4_global_scale(wl, inp, row_map) -> float:
+    """g = fp32(448 * 6 / amax(y)) over the whole tensor, from the oracle's y."""
+    o = oracle.combine(inp["expert_out"], row_map, inp["weights"], shared=inp["shared"],
+                       residual=inp["residual"], gamma=inp["gamma"], eps=wl.eps,
+                       weight_bias=wl.weight_bias, outputs=("y",))
+    amax = float(np.abs(o["y"]).max())
+    return float(np.float32(448.0 * 6.0 / amax)) if amax > 0 else 1.0
