@@ -1,0 +1,376 @@
+"""Benchmark of the MoE combine/finalize step on GB300.
+
+One step = one pass of the whole hot path over one batch: the routing build
+(moe_build_row_map: histogram, scan, stable scatter) and the combine
+(moe_combine: gather + weighted sum + shared + residual + RMSNorm + MXFP8),
+on the prefill workload T=4096, H=7168, E=256, top_k=8 (Zipf 1.1 experts,
+shared expert row, residual, RMSNorm, MXFP8 with linear UE8M0 scales).
+
+Timing: inputs resident in HBM; before every step a 256 MB buffer is written
+to flush L2 (outside the timed events); each step is bracketed by CUDA
+events on the launching stream; `value` = tokens / summed step time.  The
+combine kernel is also bracketed on its own for the roofline line.  `e2e`
+repeats the step through the same C ABI from pinned host buffers, with the
+host->device copy of the step's inputs and the device->host copy of its
+outputs inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs an independent replica on its own GPU (the
+tokens of a batch are independent; there is no data-path collective), and
+rank 0 prints one JSON line with the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE combine tokens/s and achieved HBM GB/s vs peak (T=4096,H=7168,k=8)"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["norm_quant_gb300/csrc/combine.cu", "norm_quant_gb300/csrc/ptx.cuh"]
+TRAFFIC_FILE = "profiles/combine_prefill_T4096_H7168_k8_mxfp8.md"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload():
+    from norm_quant_gb300 import synth
+    return synth.PREFILL
+
+
+def algorithmic_bytes(wl, n_valid: int) -> dict:
+    """Bytes one combine launch must move at least (reads + writes)."""
+    T, H, k = wl.T, wl.H, wl.k
+    rows = n_valid * 2 * H
+    other = (2 * H * T if wl.shared_std is not None else 0) + (2 * H * T if wl.residual else 0)
+    meta = 8 * k * T + (2 * H if wl.gamma_mean is not None else 0)
+    writes = 2 * H * T * len([o for o in wl.outputs if o in ("combined", "residual", "norm")])
+    if wl.quant == "mxfp8":
+        writes += H * T + H // 32 * T
+    elif wl.quant == "nvfp4":
+        writes += H // 2 * T + H // 16 * T
+    return {"rows": rows, "other_reads": other, "meta": meta, "writes": writes,
+            "total": rows + other + meta + writes}
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        return float(json.load(open(p))["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per combine launch from the committed ncu summary, or None
+    if the kernel source changed since those counters were taken."""
+    try:
+        text = open(os.path.join(ROOT, TRAFFIC_FILE)).read()
+    except OSError:
+        return None
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    hsh = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    if not m or not hsh or hsh.group(1) != kernel_hash():
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.p is not None:
+            time.sleep(0.2)
+            self.p.terminate()
+            out, _ = self.p.communicate(timeout=10)
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(mhz)) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def cpu_oracle_rate(wl, inp, orm, seconds: float):
+    """Tokens/s of the oracle on a bounded sample of this workload's tokens."""
+    import oracle
+    n = 16
+    while True:
+        t0 = time.perf_counter()
+        oracle.combine(inp["expert_out"], orm[:n], inp["weights"][:n], shared=inp["shared"][:n],
+                       residual=inp["residual"][:n], gamma=inp["gamma"], eps=wl.eps,
+                       weight_bias=wl.weight_bias, quant=wl.quant, sf_layout="linear",
+                       outputs=("residual", "quant"))
+        dt = time.perf_counter() - t0
+        if dt >= seconds or n >= wl.T:
+            return n / dt, n, dt
+        n = min(wl.T, max(n * 2, int(n * seconds / max(dt, 1e-3) * 1.1)))
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle timed as it stands, on the host."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from norm_quant_gb300 import synth
+    wl = workload()
+    inp = synth.make_inputs(wl)
+    st, _, _, orm, _ = oracle.build_row_map(inp["topk_ids"], wl.E)
+    rate, _, _ = cpu_oracle_rate(wl, inp, orm, 1.0)
+    budget = 90.0
+    per_step = max(1, min(wl.T, int(rate * budget / max(1, args.steps + args.warmup))))
+
+    def step(i):
+        t0 = (i * per_step) % max(1, wl.T - per_step + 1)
+        sl = slice(t0, t0 + per_step)
+        oracle.build_row_map(inp["topk_ids"][sl], wl.E)
+        oracle.combine(inp["expert_out"], orm[sl], inp["weights"][sl], shared=inp["shared"][sl],
+                       residual=inp["residual"][sl], gamma=inp["gamma"], eps=wl.eps,
+                       weight_bias=wl.weight_bias, quant=wl.quant, sf_layout="linear",
+                       outputs=("residual", "quant"))
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt
+    sample = f"{per_step} of {wl.T} tokens per step (routing build + combine of that slice)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "top_k": wl.k,
+                   "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import norm_quant_gb300 as nqg
+    from norm_quant_gb300 import synth
+    from norm_quant_gb300.build import build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build()
+    if world > 1:
+        dist.barrier()
+    build()
+    nqg.lib()
+
+    wl = workload()
+    T, H, E, k = wl.T, wl.H, wl.E, wl.k
+    inp = synth.make_inputs(wl)
+
+    def pinned(a):
+        a = a.view(np.int16) if a.dtype == np.uint16 else a
+        return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+
+    host = {n: pinned(inp[n]) for n in ("topk_ids", "weights", "expert_out", "shared", "residual", "gamma")}
+    dv = {n: t.to(dev) for n, t in host.items()}
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    row_map = torch.empty((T, k), dtype=torch.int32, device=dev)
+    ws = torch.empty(nqg.moe_build_row_map_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
+    res_out = torch.empty((T, H), dtype=torch.int16, device=dev)
+    q_out = torch.empty((T, H), dtype=torch.uint8, device=dev)
+    scales = torch.empty(nqg.moe_scales_bytes(T, H, "mxfp8"), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    args_c = nqg.combine_args(expert_out=dv["expert_out"], row_map=row_map, router_weights=dv["weights"],
+                              shared_out=dv["shared"], residual=dv["residual"], gamma=dv["gamma"],
+                              eps=wl.eps, weight_bias=wl.weight_bias, quant="mxfp8", sf_layout="linear",
+                              residual_out=res_out, quant_out=q_out, scales_out=scales)
+
+    def step(ev=None):
+        nqg.moe_build_row_map(dv["topk_ids"], E, counts, offsets, row_map, None, ws, stream=sptr)
+        if ev is not None:
+            ev[0].record(stream)
+        nqg.moe_combine(stream=sptr, args=args_c)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert nqg.moe_build_row_map_check(ws, stream=sptr) == nqg.MOE_OK
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(K):
+            flush.zero_()
+            e = ev[i]
+            e[0].record(stream)
+            step((e[1], e[2]))
+            e[3].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step_ms = np.array([e[0].elapsed_time(e[3]) for e in ev])
+    comb_ms = np.array([e[1].elapsed_time(e[2]) for e in ev])
+    total_s = step_ms.sum() / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+
+    # end to end through the C ABI from pinned host buffers
+    host_out = {"residual_out": torch.empty_like(res_out, device="cpu").pin_memory(),
+                "quant_out": torch.empty_like(q_out, device="cpu").pin_memory(),
+                "scales": torch.empty_like(scales, device="cpu").pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for n, t in host.items():
+            dv[n].copy_(t, non_blocking=True)
+        step()
+        host_out["residual_out"].copy_(res_out, non_blocking=True)
+        host_out["quant_out"].copy_(q_out, non_blocking=True)
+        host_out["scales"].copy_(scales, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    if rank == 0:
+        byt = algorithmic_bytes(wl, inp["n_valid"])
+        comb_avg_s = comb_ms.mean() / 1e3
+        achieved = byt["total"] / comb_avg_s / 1e9
+        peak, peak_kind = measured_peak()
+        line = {
+            "metric": METRIC, "value": world * T * K / total_s, "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": total_s / K * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "T": T, "H": H, "E": E, "top_k": k,
+                       "io": "bf16 in, fp32 accumulate, bf16 residual_out + MXFP8 e4m3/UE8M0 out",
+                       "l2": "256 MB L2 flush before each step, outside the timed events",
+                       "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
+            "achieved_gbs": achieved,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "kernel": "combine_kernel<4, MXFP8>", "kernel_ms": comb_avg_s * 1e3,
+                         "algorithmic_bytes": byt["total"], "traffic": recorded_traffic()},
+            "e2e": {"value": world * T * args.e2e_steps / e2e_s, "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 4 * K,
+            "clocks": clk.summary(),
+        }
+        if not args.no_cpu_baseline and world == 1:
+            import oracle
+            st, _, _, orm, _ = oracle.build_row_map(inp["topk_ids"], E)
+            rate, n, dt = cpu_oracle_rate(wl, inp, orm, args.cpu_seconds)
+            line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"first {n} of {T} tokens, combine + MXFP8 ({dt:.1f} s, 1 thread)"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

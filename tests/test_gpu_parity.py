@@ -1,0 +1,199 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle, element by
+element, on the seeded synthetic workloads and on edge cases.
+
+Routing is compared bit-exactly.  Combine outputs use the tolerances stated
+in tests/_helpers.py.  The largest workloads (T = 16384) are compared on a
+sample of token rows, which the oracle computes one by one; everything else
+is compared in full.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import norm_quant_gb300 as nqg
+import oracle
+from norm_quant_gb300 import synth
+from norm_quant_gb300.build import build
+
+from _helpers import (assert_bf16_close, assert_quant_close, d, gpu_combine, gpu_route, h,
+                      nvfp4_global_scale, oracle_combine, sum_magnitude)
+
+pytestmark = pytest.mark.gpu
+
+GAMMA_K = lambda k: (k + 3) * 2.0 ** -24  # noqa: E731
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build()
+    nqg.lib()
+
+
+def route_and_check(ids, E, stream=None):
+    st, counts, offsets, row_map, src_row = gpu_route(ids, E, stream=stream)
+    ost, oc, oo, orm, osr = oracle.build_row_map(ids, E)
+    assert st == (nqg.MOE_OK if ost == 0 else nqg.MOE_ERR_INVALID_EXPERT)
+    assert np.array_equal(h(counts), oc)
+    assert np.array_equal(h(offsets), oo)
+    assert np.array_equal(h(row_map), orm)
+    assert np.array_equal(h(src_row)[: oo[E]], osr)
+    return row_map, orm
+
+
+def compare(wl, inp, orm, got, tokens=None, global_scale=1.0):
+    T, H, k = wl.T, wl.H, wl.k
+    tok = np.arange(T) if tokens is None else np.asarray(tokens)
+    o = oracle_combine(wl, inp, orm, tokens=None if tokens is None else tok, global_scale=global_scale)
+    assert o["status"] == 0
+    mag = sum_magnitude(inp, orm, tok)
+    floor = GAMMA_K(k) * mag
+    for name in ("combined", "residual"):
+        if name in got:
+            assert_bf16_close(got[name][tok], o[name], floor, f"{wl.name}:{name}")
+    if "norm" in got:
+        res = oracle.bf16_to_f64(o["residual"])
+        rinv = 1.0 / np.sqrt((res ** 2).mean(axis=1, keepdims=True) + wl.eps)
+        g = np.abs(oracle.bf16_to_f64(inp["gamma"]) + wl.weight_bias)[None, :]
+        nfloor = 2 * floor * rinv * g + 2.0 ** -20 * np.abs(o["y"])
+        assert_bf16_close(got["norm"][tok], o["norm"], nfloor, f"{wl.name}:norm")
+    if wl.quant and "quant" in got:
+        vec = 32 if wl.quant == "mxfp8" else 16
+        Cc = H // vec
+        if tokens is None:
+            assert_quant_close(wl, got["quant"], got["scales"], o["quant"], o["scales"], T, H,
+                               global_scale, f"{wl.name}:quant")
+            if wl.sf_layout == "swizzled":
+                # every byte outside the real (row, column) cells is zero padding
+                used = np.zeros(got["scales"].size, bool)
+                used[oracle.sf_offsets(T, Cc, "swizzled").ravel()] = True
+                assert np.all(got["scales"][~used] == 0)
+        else:
+            lin = got["scales"][oracle.sf_offsets(T, Cc, wl.sf_layout)][tok].ravel()
+            assert_quant_close(wl, got["quant"][tok], lin, o["quant"], o["scales"], tok.size, H,
+                               global_scale, f"{wl.name}:quant", layout="linear")
+
+
+def run_workload(wl, sample=None, canary=False):
+    inp = synth.make_inputs(wl)
+    d_rm, orm = route_and_check(inp["topk_ids"], wl.E)
+    g = nvfp4_global_scale(wl, inp, orm) if wl.quant == "nvfp4" else 1.0
+    got = gpu_combine(wl, inp, d_rm, global_scale=g, canary=canary)
+    assert got["status"] == 0
+    tokens = None
+    if sample is not None and wl.T > sample:
+        rng = np.random.Generator(np.random.PCG64(wl.seed + 7))
+        tokens = np.unique(np.concatenate([[0, wl.T - 1], rng.choice(wl.T, sample, replace=False)]))
+    compare(wl, inp, orm, got, tokens=tokens, global_scale=g)
+    return inp, orm, got
+
+
+# ---------------------------------------------------------------- workloads
+
+@pytest.mark.parametrize("wl", synth.WORKLOADS, ids=lambda w: w.name)
+def test_workload_parity(wl):
+    run_workload(wl, sample=384 if wl.T > 8192 else None, canary=wl.T <= 4096)
+
+
+@pytest.mark.parametrize("T", synth.SWEEP_T)
+def test_padded_sweep_parity(T):
+    run_workload(synth.sweep_point(T), sample=256 if T > 4096 else None)
+
+
+# -------------------------------------------------------------- edge cases
+
+def _wl(**kw):
+    base = dict(name="edge", T=37, H=256, E=16, k=4, residual=True, gamma_mean=1.0,
+                outputs=("combined", "residual", "norm"), seed=77)
+    base.update(kw)
+    return synth.Workload(**base)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(k=1), dict(k=32, E=64), dict(E=1, k=1), dict(H=8, outputs=("combined",), gamma_mean=None),
+    dict(H=32, quant="mxfp8", outputs=("combined", "quant")),
+    dict(H=16, quant="nvfp4", outputs=("residual", "quant"), gamma_mean=0.0, weight_bias=1.0),
+    dict(H=7200, T=19, quant="mxfp8", outputs=("residual", "norm", "quant")),   # ragged last slot
+    dict(H=16384, T=9, k=8, E=32, quant="mxfp8", outputs=("residual", "quant")),  # largest H
+    dict(H=8192, T=13, quant="nvfp4", sf_layout="swizzled", outputs=("residual", "quant")),
+    dict(H=96, T=130, quant="mxfp8", sf_layout="swizzled", outputs=("norm", "quant")),  # C = 3 pads
+    dict(H=48, T=200, quant="nvfp4", sf_layout="swizzled", outputs=("combined", "quant")),
+    dict(pad_frac=1.0, shared_std=0.5, quant="mxfp8", outputs=("combined", "residual", "quant")),
+    dict(pad_frac=0.5, outputs=("combined", "residual", "norm")),
+    dict(T=1, H=7168, E=256, k=8, shared_std=0.5, quant="mxfp8", outputs=("residual", "norm", "quant")),
+    dict(T=3000, H=512, E=8, k=8, dist="zipf", zipf_s=2.0, weight_bias=0.375),
+    dict(eps=0.5, gamma_std=1.0),
+], ids=lambda kw: ",".join(f"{a}={b}" for a, b in kw.items()))
+def test_edge_parity(kw):
+    wl = _wl(**kw)
+    inp = synth.make_inputs(wl)
+    d_rm, orm = route_and_check(inp["topk_ids"], wl.E)
+    g = nvfp4_global_scale(wl, inp, orm) if wl.quant == "nvfp4" else 1.0
+    got = gpu_combine(wl, inp, d_rm, global_scale=g, canary=True)
+    assert got["status"] == 0
+    compare(wl, inp, orm, got, global_scale=g)
+
+
+def test_duplicate_experts_in_a_token():
+    rng = np.random.Generator(np.random.PCG64(5))
+    ids = rng.integers(0, 4, (300, 8)).astype(np.int32)
+    ids[rng.random((300, 8)) < 0.1] = -1
+    route_and_check(ids, 4)
+
+
+def test_routing_sizes_and_determinism():
+    rng = np.random.Generator(np.random.PCG64(6))
+    for T, k, E in [(1, 1, 1), (3, 2, 8192), (1000, 32, 5), (5000, 8, 1024), (70000, 2, 3)]:
+        ids = rng.integers(-1, E, (T, k)).astype(np.int32)
+        a = route_and_check(ids, E)[0]
+        b = gpu_route(ids, E)[3]
+        assert torch.equal(a, b)
+
+
+def test_invalid_expert_ids_are_flagged():
+    ids = np.array([[0, 1], [9, -1], [-5, 2]], np.int32)
+    st, counts, offsets, row_map, _ = gpu_route(ids, 4)
+    assert st == nqg.MOE_ERR_INVALID_EXPERT
+    assert h(row_map).tolist() == [[0, 1], [-1, -1], [-1, 2]]
+    assert h(counts).tolist() == [1, 1, 1, 0]
+
+
+def test_empty_batch_is_a_noop():
+    st, counts, offsets, row_map, _ = gpu_route(np.zeros((0, 4), np.int32), 8)
+    assert st == 0 and h(counts).tolist() == [0] * 8 and h(offsets).tolist() == [0] * 9
+    out = torch.full((16,), 0x1234, dtype=torch.int16, device="cuda")
+    nqg.moe_combine(expert_out=torch.zeros((0, 64), dtype=torch.int16, device="cuda"),
+                    row_map=torch.zeros((0, 2), dtype=torch.int32, device="cuda"),
+                    router_weights=torch.zeros((0, 2), dtype=torch.float32, device="cuda"),
+                    combined_out=out, H=64)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0x1234)
+
+
+def test_row_out_of_range_is_reported_and_skipped():
+    wl = _wl(T=8, H=64, outputs=("combined",), residual=False, gamma_mean=None)
+    inp = synth.make_inputs(wl)
+    _, orm = route_and_check(inp["topk_ids"], wl.E)
+    bad = orm.copy()
+    bad[2, 1] = inp["n_valid"] + 5
+    got = gpu_combine(wl, inp, d(bad))
+    assert got["status"] == nqg.MOE_ERR_ROW_OUT_OF_RANGE
+    skip = orm.copy()
+    skip[2, 1] = -1
+    o = oracle_combine(wl, inp, skip)
+    assert_bf16_close(got["combined"], o["combined"], GAMMA_K(wl.k) * sum_magnitude(inp, skip, range(8)),
+                      "skipped slot")
+
+
+def test_repeat_runs_identical_and_side_stream():
+    wl = dataclasses.replace(synth.PREFILL, T=700, name="repeat")
+    inp = synth.make_inputs(wl)
+    d_rm, orm = route_and_check(inp["topk_ids"], wl.E)
+    a = gpu_combine(wl, inp, d_rm)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        d_rm2, _ = route_and_check(inp["topk_ids"], wl.E, stream=s)
+        b = gpu_combine(wl, inp, d_rm2, stream=s)
+    for key in ("residual", "quant", "scales"):
+        assert np.array_equal(a[key], b[key])
