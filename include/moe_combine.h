@@ -176,8 +176,9 @@ typedef struct moe_combine_args {
  * the quantiser reads x directly.  Without residual, x = s.
  * Padded tokens (all slots -1) are still written: s = shared (or 0).
  * Host-side validation, before any launch:
- *   args non-NULL; T >= 0; H % 8 == 0 and 8 <= H <= MOE_MAX_HIDDEN;
- *   1 <= top_k <= MOE_MAX_TOP_K; row_map, router_weights non-NULL;
+ *   args non-NULL; T >= 0; reserved0 == 0; H % 8 == 0 and 8 <= H <= MOE_MAX_HIDDEN;
+ *   1 <= top_k <= MOE_MAX_TOP_K; T == 0 then returns MOE_OK without looking at
+ *   any pointer (empty tensors may carry NULL); otherwise row_map, router_weights non-NULL;
  *   expert_out non-NULL when n_expert_rows > 0; every bf16 / byte tensor
  *   pointer 16-byte aligned; at least one output requested;
  *   norm_out needs gamma; quant in {NONE, MXFP8, NVFP4}; MXFP8 needs

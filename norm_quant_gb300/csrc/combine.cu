@@ -33,6 +33,7 @@
 // Every wait is bounded (kWaitLimitNs); a wait that gives up records
 // MOE_ERR_DEVICE_TIMEOUT and the CTA drains its own copies and returns.
 #include <cstdint>
+#include <cstdlib>
 #include <cuda_runtime.h>
 
 #include "common.h"
@@ -459,15 +460,29 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) combine_kerne
 // ------------------------------------------------------------------- host
 
 struct Plan {
-    int vpt, ncw, stages;
+    int vpt, ncw, stages, ctas_per_sm;
     SmemLayout smem;
 };
+
+// Tuning knobs (environment, read once): NQG_COMBINE_CTAS_PER_SM (1..4,
+// default 1) splits the shared-memory budget between that many resident
+// CTAs per SM; NQG_COMBINE_STAGES caps the ring depth.
+int env_int(const char *name, int dflt, int lo, int hi)
+{
+    const char *v = std::getenv(name);
+    if (!v || !*v)
+        return dflt;
+    const int x = std::atoi(v);
+    return x < lo ? lo : (x > hi ? hi : x);
+}
 
 // Vectors per consumer thread: the smallest of 1, 2, 4, 8 that covers the
 // row with at most kMaxConsumerWarps consumer warps; ring depth: as many
 // whole rows as fit the shared-memory budget, 2..32.
 Plan make_plan(int32_t H)
 {
+    static const int ctas_per_sm = env_int("NQG_COMBINE_CTAS_PER_SM", 1, 1, 4);
+    static const int max_stages = env_int("NQG_COMBINE_STAGES", kMaxStages, 2, kMaxStages);
     Plan pl{};
     const int nvec = H / 8;
     pl.vpt = 8;
@@ -481,8 +496,11 @@ Plan make_plan(int32_t H)
     const SmemLayout one = smem_layout(H, 1, pl.ncw);
     const size_t fixed = one.total - one.row_stride - 16 - sizeof(StageMeta);
     const size_t per_stage = one.row_stride + 16 + sizeof(StageMeta);
-    const int s = static_cast<int>((kSmemBudget - fixed) / per_stage);
-    pl.stages = s < 2 ? 2 : (s > kMaxStages ? kMaxStages : s);
+    // one CTA keeps kSmemBudget; several share the SM's 228 KB (1 KB reserved each)
+    const size_t budget = ctas_per_sm == 1 ? kSmemBudget : (224 * 1024) / ctas_per_sm - 2048;
+    const int s = static_cast<int>((budget - fixed) / per_stage);
+    pl.stages = s < 2 ? 2 : (s > max_stages ? max_stages : s);
+    pl.ctas_per_sm = ctas_per_sm;
     pl.smem = smem_layout(H, pl.stages, pl.ncw);
     return pl;
 }
@@ -502,7 +520,7 @@ moe_status launch_t(const Params &p, const Plan &pl, cudaStream_t stream)
         if (dev >= 0 && dev < 64)
             configured_for[dev] = need;
     }
-    const int64_t ctas = sm_count();
+    const int64_t ctas = static_cast<int64_t>(sm_count()) * pl.ctas_per_sm;
     if (ctas <= 0)
         return MOE_ERR_CUDA;
     const int grid = static_cast<int>(p.T < ctas ? p.T : ctas);
@@ -536,6 +554,8 @@ extern "C" moe_status moe_combine(const moe_combine_args *a, moe_stream_t stream
         return MOE_ERR_INVALID_ARG;
     if (a->H > MOE_MAX_HIDDEN || a->top_k > MOE_MAX_TOP_K)
         return MOE_ERR_UNSUPPORTED;
+    if (a->T == 0)
+        return MOE_OK;  // an empty batch: empty tensors may carry NULL pointers
     if (!a->row_map || !a->router_weights || a->n_expert_rows < 0)
         return MOE_ERR_INVALID_ARG;
     if (a->n_expert_rows > 0 && !a->expert_out)
@@ -567,8 +587,6 @@ extern "C" moe_status moe_combine(const moe_combine_args *a, moe_stream_t stream
     if ((reinterpret_cast<uintptr_t>(a->row_map) & 3u) || (reinterpret_cast<uintptr_t>(a->router_weights) & 3u) ||
         (reinterpret_cast<uintptr_t>(a->status) & 3u))
         return MOE_ERR_INVALID_ARG;
-    if (a->T == 0)
-        return MOE_OK;
 
     Params p{};
     p.T = a->T;

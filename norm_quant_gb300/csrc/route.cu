@@ -14,6 +14,14 @@
 // Ranks come from __match_any_sync over 32 slots at a time plus a running
 // per-expert count in shared memory, so the result is deterministic and
 // bit-exact: no atomics decide a position.  No kernel waits on another CTA.
+//
+// For N <= kFusedMaxSlots and E <= kFusedMaxExperts the three steps run as
+// ONE launch (route_fused_kernel): a thread-block cluster of up to 8 CTAs of
+// 32 warps, one chunk per warp.  Each CTA keeps its chunk histograms in
+// shared memory; after a cluster barrier every CTA reads the per-expert
+// totals of the others through distributed shared memory, derives offsets
+// and its own chunk bases, and scatters.  Cluster barriers are hardware
+// barriers over co-scheduled CTAs, so nothing spins.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -41,6 +49,11 @@ WorkspaceLayout layout_for(int64_t N, int32_t E)
     L.total = L.hist_off + static_cast<size_t>(L.chunks) * static_cast<size_t>(E) * sizeof(int32_t);
     L.total = (L.total + 255) / 256 * 256;
     return L;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
 int warps_per_cta(int32_t E)
@@ -221,6 +234,240 @@ __global__ void route_scatter_kernel(const int32_t *__restrict__ ids, int64_t N,
     }
 }
 
+
+constexpr int kFusedThreads = 1024;
+constexpr int kFusedWarps = kFusedThreads / 32;
+constexpr int kFusedMaxCtas = 8;                 // portable cluster size
+constexpr int kFusedMaxPerLane = 32;             // chunk <= 1024 slots
+constexpr int64_t kFusedMaxSlots = int64_t(kFusedMaxCtas) * kFusedWarps * 32 * kFusedMaxPerLane;
+constexpr int kFusedMaxExperts = 1024;
+
+struct FusedPlan {
+    int ctas, chunk;  // chunk: slots per warp, a multiple of 32
+    size_t smem;
+};
+
+FusedPlan fused_plan(int64_t N, int32_t E)
+{
+    FusedPlan f{};
+    const int64_t per_cta_at_256 = int64_t(kFusedWarps) * 256;
+    int64_t ctas = (N + per_cta_at_256 - 1) / per_cta_at_256;
+    f.ctas = static_cast<int>(ctas < 1 ? 1 : (ctas > kFusedMaxCtas ? kFusedMaxCtas : ctas));
+    const int64_t warps = int64_t(f.ctas) * kFusedWarps;
+    f.chunk = static_cast<int>(((N + warps - 1) / warps + 31) / 32 * 32);
+    if (f.chunk < 32)
+        f.chunk = 32;
+    // hist[32][E] + tot[E] + cnt[E] + pre[E] + off[E + 1] + warp sums[32]
+    f.smem = (static_cast<size_t>(kFusedWarps) * E + 4 * static_cast<size_t>(E) + 1 + 32) * sizeof(int32_t);
+    return f;
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Reads the int32 at the same shared-memory offset as `local` in CTA `rank`
+// of this cluster.
+__device__ __forceinline__ int32_t ld_dsmem(const int32_t *local, uint32_t rank)
+{
+    uint32_t remote, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+    return static_cast<int32_t>(v);
+}
+
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    route_fused_kernel(const int32_t *__restrict__ ids, int64_t N, int32_t E, int32_t chunk,
+                       int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                       int32_t *__restrict__ row_map, int32_t *__restrict__ src_row, int32_t *__restrict__ err)
+{
+    extern __shared__ int32_t sh[];
+    int32_t *hist = sh;                                     // [32][E]
+    int32_t *tot = hist + static_cast<size_t>(kFusedWarps) * E;  // [E] this CTA's totals (read remotely)
+    int32_t *cnt = tot + E;                                 // [E] cluster-wide counts
+    int32_t *pre = cnt + E;                                 // [E] counts of lower-ranked CTAs
+    int32_t *off = pre + E;                                 // [E + 1] offsets
+    int32_t *wsum = off + E + 1;                            // [32] scan scratch
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t nctas = gridDim.x;  // the whole grid is one cluster
+    const int per_lane = chunk >> 5;
+    const int64_t first = (static_cast<int64_t>(rank) * kFusedWarps + warp) * chunk;
+
+    // 1. chunk histograms (every thread reaches every barrier below)
+    int32_t *h = hist + static_cast<size_t>(warp) * E;
+    for (int e = lane; e < E; e += 32)
+        h[e] = 0;
+    __syncwarp();
+    int32_t v[kFusedMaxPerLane];
+    bool bad = false;
+#pragma unroll
+    for (int it = 0; it < kFusedMaxPerLane; ++it) {
+        const int64_t i = first + it * 32 + lane;
+        v[it] = (it < per_lane && i < N) ? __ldg(ids + i) : -1;
+    }
+#pragma unroll
+    for (int it = 0; it < kFusedMaxPerLane; ++it) {
+        const int32_t e = v[it];
+        if (e >= 0 && e < E)
+            atomicAdd(&h[e], 1);
+        else if (e != -1)
+            bad = true;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0)
+        atomicOr(err, 1);
+    __syncthreads();
+    // 2. per-expert exclusive prefix over this CTA's warps; CTA totals
+    for (int e = threadIdx.x; e < E; e += kFusedThreads) {
+        int32_t run = 0;
+        for (int w = 0; w < kFusedWarps; ++w) {
+            const int32_t x = hist[static_cast<size_t>(w) * E + e];
+            hist[static_cast<size_t>(w) * E + e] = run;
+            run += x;
+        }
+        tot[e] = run;
+    }
+    // 3. publish totals to the cluster
+    cluster_sync_all();
+    for (int e = threadIdx.x; e < E; e += kFusedThreads) {
+        int32_t all = 0, before = 0;
+        for (uint32_t b = 0; b < nctas; ++b) {
+            const int32_t x = (b == rank) ? tot[e] : ld_dsmem(tot + e, b);
+            all += x;
+            before += (b < rank) ? x : 0;
+        }
+        cnt[e] = all;
+        pre[e] = before;
+    }
+    // 4. no CTA reads another's shared memory after this barrier, so any CTA
+    //    may run ahead and exit
+    cluster_sync_all();
+    // 5. exclusive scan of cnt over experts (one contiguous range per thread)
+    {
+        const int per_t = (E + kFusedThreads - 1) / kFusedThreads;
+        const int e0 = threadIdx.x * per_t, e1 = (e0 + per_t < E) ? e0 + per_t : E;
+        int32_t s = 0;
+        for (int e = e0; e < e1; ++e)
+            s += cnt[e];
+        int32_t incl = s;
+#pragma unroll
+        for (int dd = 1; dd < 32; dd <<= 1) {
+            const int32_t o = __shfl_up_sync(0xffffffffu, incl, dd);
+            if (lane >= dd)
+                incl += o;
+        }
+        if (lane == 31)
+            wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int32_t ws = wsum[lane];
+            int32_t wi = ws;
+#pragma unroll
+            for (int dd = 1; dd < 32; dd <<= 1) {
+                const int32_t o = __shfl_up_sync(0xffffffffu, wi, dd);
+                if (lane >= dd)
+                    wi += o;
+            }
+            wsum[lane] = wi - ws;  // exclusive prefix of warp sums
+            if (lane == 31)
+                off[E] = wi;
+        }
+        __syncthreads();
+        int32_t run = wsum[warp] + incl - s;
+        for (int e = e0; e < e1; ++e) {
+            off[e] = run;
+            run += cnt[e];
+        }
+    }
+    __syncthreads();
+    if (rank == 0) {
+        for (int e = threadIdx.x; e < E; e += kFusedThreads) {
+            counts[e] = cnt[e];
+            offsets[e] = off[e];
+        }
+        if (threadIdx.x == 0)
+            offsets[E] = off[E];
+    }
+    // 6. chunk bases
+    for (int idx = threadIdx.x; idx < kFusedWarps * E; idx += kFusedThreads) {
+        const int e = idx % E;
+        hist[idx] += off[e] + pre[e];
+    }
+    __syncthreads();
+    // 7. stable scatter of this warp's chunk
+    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int it = 0; it < kFusedMaxPerLane; ++it) {
+        if (it >= per_lane)
+            break;
+        const int64_t i = first + it * 32 + lane;
+        const int32_t e = v[it];
+        const bool valid = (e >= 0) && (e < E);
+        const uint32_t peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+        const int r = __popc(peers & lt);
+        if (valid) {
+            const int32_t row = h[e] + r;
+            row_map[i] = row;
+            if (src_row)
+                src_row[row] = static_cast<int32_t>(i);
+        } else if (i < N) {
+            row_map[i] = -1;
+        }
+        __syncwarp();
+        if (valid && r == 0)
+            h[e] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+// Whether one cluster of f.ctas CTAs with f.smem bytes of shared memory can
+// be placed on this device (cached per device, cluster size and smem size).
+bool fused_launchable(const FusedPlan &f)
+{
+    constexpr int kBuckets = 8;
+    static int cache[64][kFusedMaxCtas + 1][kBuckets];  // 0 unknown, 1 yes, 2 no
+    static bool attr_set[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return false;
+    const int bucket = static_cast<int>((f.smem + 32 * 1024 - 1) / (32 * 1024));  // <= 5 for E <= 1024
+    if (bucket >= kBuckets)
+        return false;
+    if (cache[dev][f.ctas][bucket])
+        return cache[dev][f.ctas][bucket] == 1;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(route_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kBuckets * 32 * 1024 - 1024) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        attr_set[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = f.ctas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(f.ctas);
+    cfg.blockDim = dim3(kFusedThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(bucket) * 32 * 1024;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const bool ok = cudaOccupancyMaxActiveClusters(&n, route_fused_kernel, &cfg) == cudaSuccess && n > 0;
+    cudaGetLastError();
+    cache[dev][f.ctas][bucket] = ok ? 1 : 2;
+    return ok;
+}
 } // namespace
 } // namespace nqg
 
@@ -270,6 +517,29 @@ extern "C" moe_status moe_build_row_map(const int32_t *topk_ids, int64_t T, int3
             cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess)
             return MOE_ERR_CUDA;
         return MOE_OK;
+    }
+    if (N <= kFusedMaxSlots && E <= kFusedMaxExperts) {
+        const FusedPlan f = fused_plan(N, E);
+        if (fused_launchable(f)) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = f.ctas;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(f.ctas);
+            cfg.blockDim = dim3(kFusedThreads);
+            cfg.dynamicSmemBytes = f.smem;
+            cfg.stream = s;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaLaunchKernelEx(&cfg, route_fused_kernel, topk_ids, N, E, f.chunk, counts, offsets, row_map,
+                                   src_row, err) != cudaSuccess) {
+                cudaGetLastError();
+                return MOE_ERR_CUDA;
+            }
+            return MOE_OK;
+        }
     }
     const int wpc = warps_per_cta(E);
     const int grid = static_cast<int>((L.chunks + wpc - 1) / wpc);

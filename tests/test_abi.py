@@ -81,6 +81,7 @@ def _args(**kw):
     (dict(row_map=0x2002), 1), (dict(eps=-1.0), 1), (dict(eps=float("nan")), 1),
     (dict(reserved0=1), 1), (dict(status=0x8002), 1),
     (dict(T=0), 0),  # a valid no-op: returns before any CUDA call
+    (dict(T=0, row_map=None, router_weights=None, expert_out=None, combined_out=None), 0),
 ])
 def test_combine_validation(L, kw, want):
     a = _args(**kw)

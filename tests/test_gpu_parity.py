@@ -144,7 +144,9 @@ def test_duplicate_experts_in_a_token():
 
 def test_routing_sizes_and_determinism():
     rng = np.random.Generator(np.random.PCG64(6))
-    for T, k, E in [(1, 1, 1), (3, 2, 8192), (1000, 32, 5), (5000, 8, 1024), (70000, 2, 3)]:
+    # single-launch cluster path and (E > 1024 or N > 262144) the three-kernel path
+    for T, k, E in [(1, 1, 1), (3, 2, 8192), (1000, 32, 5), (5000, 8, 1024), (70000, 2, 3),
+                    (40000, 8, 256), (33000, 8, 16), (2000, 8, 2048), (32768, 8, 256)]:
         ids = rng.integers(-1, E, (T, k)).astype(np.int32)
         a = route_and_check(ids, E)[0]
         b = gpu_route(ids, E)[3]
