@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload", choices=["tiny", "decode", "prefill", "gemma", "padded"],
+                    default="prefill", help="the headline is prefill; the others are for analysis")
     ap.add_argument("--l2", choices=["none", "write"], default="none",
                     help="none: inputs larger than L2; write: 256 MB write before each step")
     return ap.parse_args()
@@ -66,9 +68,10 @@ def dist_env():
     return rank, world, local
 
 
-def workload():
+def workload(name="prefill"):
     from norm_quant_gb300 import synth
-    return synth.PREFILL
+    return {"tiny": synth.TINY, "decode": synth.DECODE, "prefill": synth.PREFILL,
+            "gemma": synth.GEMMA_NVFP4, "padded": synth.PADDED}[name]
 
 
 def algorithmic_bytes(wl, n_valid: int) -> dict:
@@ -185,7 +188,7 @@ def run_reference(args):
         return
     import oracle
     from norm_quant_gb300 import synth
-    wl = workload()
+    wl = workload(args.workload)
     inp = synth.make_inputs(wl)
     st, _, _, orm, _ = oracle.build_row_map(inp["topk_ids"], wl.E)
     rate, _, _ = cpu_oracle_rate(wl, inp, orm, 1.0)
@@ -242,7 +245,7 @@ def run_ours(args):
     build()
     nqg.lib()
 
-    wl = workload()
+    wl = workload(args.workload)
     T, H, E, k = wl.T, wl.H, wl.E, wl.k
     inp = synth.make_inputs(wl)
 
@@ -250,22 +253,32 @@ def run_ours(args):
         a = a.view(np.int16) if a.dtype == np.uint16 else a
         return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
 
-    host = {n: pinned(inp[n]) for n in ("topk_ids", "weights", "expert_out", "shared", "residual", "gamma")}
+    names = [n for n in ("topk_ids", "weights", "expert_out", "shared", "residual", "gamma")
+             if inp[n] is not None]
+    host = {n: pinned(inp[n]) for n in names}
     dv = {n: t.to(dev) for n, t in host.items()}
     counts = torch.empty(E, dtype=torch.int32, device=dev)
     offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
     row_map = torch.empty((T, k), dtype=torch.int32, device=dev)
     ws = torch.empty(nqg.moe_build_row_map_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
-    res_out = torch.empty((T, H), dtype=torch.int16, device=dev)
-    q_out = torch.empty((T, H), dtype=torch.uint8, device=dev)
-    scales = torch.empty(nqg.moe_scales_bytes(T, H, "mxfp8"), dtype=torch.uint8, device=dev)
+    outs = {}
+    for o in ("combined", "residual", "norm"):
+        if o in wl.outputs:
+            outs[o] = torch.empty((T, H), dtype=torch.int16, device=dev)
+    if wl.quant:
+        outs["quant"] = torch.empty((T, H if wl.quant == "mxfp8" else H // 2), dtype=torch.uint8, device=dev)
+        outs["scales"] = torch.empty(nqg.moe_scales_bytes(T, H, wl.quant, wl.sf_layout), dtype=torch.uint8,
+                                     device=dev)
     flush = torch.empty(L2_FLUSH_BYTES if args.l2 == "write" else 16, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
+    # NVFP4's per-tensor scale only changes which codes come out, not the work
     args_c = nqg.combine_args(expert_out=dv["expert_out"], row_map=row_map, router_weights=dv["weights"],
-                              shared_out=dv["shared"], residual=dv["residual"], gamma=dv["gamma"],
-                              eps=wl.eps, weight_bias=wl.weight_bias, quant="mxfp8", sf_layout="linear",
-                              residual_out=res_out, quant_out=q_out, scales_out=scales)
+                              shared_out=dv.get("shared"), residual=dv.get("residual"), gamma=dv.get("gamma"),
+                              eps=wl.eps, weight_bias=wl.weight_bias, quant=wl.quant, sf_layout=wl.sf_layout,
+                              global_scale=1.0, combined_out=outs.get("combined"),
+                              residual_out=outs.get("residual"), norm_out=outs.get("norm"),
+                              quant_out=outs.get("quant"), scales_out=outs.get("scales"), H=H)
 
     def step(ev=None):
         nqg.moe_build_row_map(dv["topk_ids"], E, counts, offsets, row_map, None, ws, stream=sptr)
@@ -307,9 +320,7 @@ def run_ours(args):
         total_s = float(t.item())
 
     # end to end through the C ABI from pinned host buffers
-    host_out = {"residual_out": torch.empty_like(res_out, device="cpu").pin_memory(),
-                "quant_out": torch.empty_like(q_out, device="cpu").pin_memory(),
-                "scales": torch.empty_like(scales, device="cpu").pin_memory()}
+    host_out = {n: torch.empty_like(t, device="cpu").pin_memory() for n, t in outs.items()}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
 
@@ -317,9 +328,8 @@ def run_ours(args):
         for n, t in host.items():
             dv[n].copy_(t, non_blocking=True)
         step()
-        host_out["residual_out"].copy_(res_out, non_blocking=True)
-        host_out["quant_out"].copy_(q_out, non_blocking=True)
-        host_out["scales"].copy_(scales, non_blocking=True)
+        for n, t in outs.items():
+            host_out[n].copy_(t, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -347,7 +357,8 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": wl.name, "T": T, "H": H, "E": E, "top_k": k,
-                       "io": "bf16 in, fp32 accumulate, bf16 residual_out + MXFP8 e4m3/UE8M0 out",
+                       "io": f"bf16 in, fp32 accumulate, out: {'+'.join(wl.outputs)}"
+                             + (f" ({wl.quant}, {wl.sf_layout} scales)" if wl.quant else ""),
                        "l2": ("256 MB L2 write-flush before each step, outside the timed events"
                               if args.l2 == "write" else
                               "no flush: each step streams 676 MB through the 129 MB L2"),
@@ -355,14 +366,14 @@ def run_ours(args):
             "achieved_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
-                         "kernel": "combine_kernel<4, MXFP8>", "kernel_ms": comb_avg_s * 1e3,
+                         "kernel": "combine_kernel", "kernel_ms": comb_avg_s * 1e3,
                          "algorithmic_bytes": byt["total"], "traffic": recorded_traffic()},
             "e2e": {"value": world * T * args.e2e_steps / e2e_s, "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 4 * K,
             "clocks": clk.summary(),
         }
-        if not args.no_cpu_baseline and world == 1:
+        if not args.no_cpu_baseline and world == 1 and wl.residual and wl.shared_std is not None:
             import oracle
             st, _, _, orm, _ = oracle.build_row_map(inp["topk_ids"], E)
             rate, n, dt = cpu_oracle_rate(wl, inp, orm, args.cpu_seconds)

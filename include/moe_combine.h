@@ -188,6 +188,21 @@ typedef struct moe_combine_args {
  * MOE_ERR_CUDA. */
 moe_status moe_combine(const moe_combine_args *args, moe_stream_t stream);
 
+/* Overrides the combine kernel's launch plan for the rest of the process
+ * (performance only: every plan computes identical results).  Each argument
+ * 0 restores the automatic choice:
+ *   vpt            8-element vectors per consumer thread: 1, 2, 4 or 8
+ *                  (ignored where it cannot cover H; at most 28, 16, 8, 8
+ *                  consumer warps respectively);
+ *   rows_per_slot  rows staged per ring slot, 1..4 (capped at 4 for vpt <= 2,
+ *                  2 for vpt 4, 1 for vpt 8);
+ *   ring_kib       shared-memory ring size in KiB, 1..224 (capped to what fits);
+ *   ctas_per_sm    resident CTAs per SM the grid is sized for, 1..4.
+ * Not synchronised with calls in flight on other host threads.  Returns
+ * MOE_OK or MOE_ERR_INVALID_ARG.  (No counterpart on the pages: a tuning
+ * hook of this implementation.) */
+moe_status moe_tuning_set(int32_t vpt, int32_t rows_per_slot, int32_t ring_kib, int32_t ctas_per_sm);
+
 /* Bytes of the scale matrix for T rows of H elements: linear T * C, swizzled
  * roundup(T, 128) * roundup(C, 4), with C = H / 32 (MXFP8) or H / 16 (NVFP4). */
 moe_status moe_scales_bytes(int64_t T, int32_t H, int32_t quant, int32_t sf_layout,

@@ -1,4 +1,4 @@
-// combine.cu -- the MoE combine/finalize kernel and its C entry point.
+// combine.cu -- the MoE combine/finalize kernel and its C entry points.
 //
 // What it computes (Struct_ep_combine_skip_a2a, execute: weighted sum of
 // routed expert outputs; fused_shared_expert; flashinfer.comm.
@@ -17,23 +17,23 @@
 //
 // Design (an HBM-bound gather; no tensor cores -- nothing here is a
 // contraction):
-//   * persistent CTAs, one per SM; token t goes to CTA t mod gridDim;
-//   * one producer warp walks the CTA's tokens and, for each row the token
-//     needs (its valid expert rows in ascending j, then the shared row, then
-//     the residual row), issues ONE cp.async.bulk of the whole 2H-byte row
-//     into the next slot of a ring of `stages` shared-memory row buffers,
-//     completing on that slot's "full" mbarrier; row_map / weights of the
-//     next token are prefetched while the current one is issued;
-//   * consumer warps own 8-element vectors v = slot * NC + thread of the row
-//     and accumulate fp32 in registers straight from the ring, then release
-//     the slot on its "empty" mbarrier;
-//   * after a token's last row: bf16 stores, a sum of squares reduced by warp
-//     shuffles and an mbarrier-synchronised cross-warp sum, the norm, and the
-//     block quantiser (an MXFP8 block is 4 consecutive lanes, NVFP4 2).
+//   * persistent CTAs, one per SM by default; token t goes to CTA t mod grid;
+//   * one producer warp walks the CTA's tokens.  A token needs its valid
+//     expert rows in ascending j, then the shared row, then the residual row;
+//     the producer packs up to R of them into one slot of a shared-memory
+//     ring (one cp.async.bulk per 2H-byte row, all completing on the slot's
+//     "full" mbarrier) and writes the slot's weights and flags beside it;
+//     row_map / weights of the next token are prefetched meanwhile;
+//   * consumer warps own 8-element vectors v = slot * NC + thread of the row;
+//     per ring slot they wait once, load all R rows' vectors (R * VPT
+//     independent 16-byte shared loads), accumulate fp32 in registers in
+//     row order, and release the slot on its "empty" mbarrier;
+//   * after a token's last slot: bf16 stores, a sum of squares reduced by
+//     warp shuffles and an mbarrier-synchronised cross-warp sum, the norm,
+//     and the block quantiser (an MXFP8 block is 4 consecutive lanes, NVFP4 2).
 // Every wait is bounded (kWaitLimitNs); a wait that gives up records
 // MOE_ERR_DEVICE_TIMEOUT and the CTA drains its own copies and returns.
 #include <cstdint>
-#include <cstdlib>
 #include <cuda_runtime.h>
 
 #include "common.h"
@@ -43,17 +43,29 @@ namespace nqg {
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr int kMaxConsumerWarps = 8;  // with VPT <= 8 this covers H <= 16384
 constexpr int kMaxStages = 32;
 constexpr size_t kSmemBudget = 200 * 1024;
+constexpr size_t kDefaultRingBytes = 144 * 1024;
 
-enum : int32_t { F_EXPERT = 1, F_SHARED = 2, F_RESIDUAL = 4, F_LAST = 8, F_EMPTY = 16 };
+// Consumer warps allowed per CTA for each VPT (vectors of 8 elements per
+// consumer thread); the CTA adds one producer warp.  Together they cover
+// H <= 7168 (VPT 1), 8192 (VPT 2, 4) and 16384 (VPT 8).
+template <int VPT>
+constexpr int max_consumer_warps() { return VPT == 1 ? 28 : (VPT == 2 ? 16 : 8); }
+inline int max_consumer_warps_rt(int vpt) { return vpt == 1 ? 28 : (vpt == 2 ? 16 : 8); }
+// Rows a ring slot may hold, bounded by the registers the loads take.
+template <int VPT>
+constexpr int max_rows() { return VPT <= 2 ? 4 : (VPT == 4 ? 2 : 1); }
+inline int max_rows_rt(int vpt) { return vpt <= 2 ? 4 : (vpt == 4 ? 2 : 1); }
+
+enum : int32_t { F_LAST = 1, F_RESID = 2 };
 
 struct StageMeta {
     int32_t t;
-    float w;
-    int32_t flags;
+    int32_t n;      // rows in the slot, 0..R
+    int32_t flags;  // F_LAST: the token's last slot; F_RESID: its last row is the residual
     int32_t pad;
+    float w[4];     // weight of each row (1 for the shared and residual rows)
 };
 
 struct Params {
@@ -71,19 +83,20 @@ struct Params {
     uint16_t *combined_out, *residual_out, *norm_out;
     uint8_t *quant_out, *scales_out;
     int32_t *status;
-    int32_t stages;
+    int32_t stages, rows;  // ring slots, rows per slot
     int64_t sf_cols, sf_cols_pad, sf_rows_pad;
 };
 
 struct SmemLayout {
-    uint32_t row_stride, bars, meta, red, total;
+    uint32_t row_stride, slot_stride, bars, meta, red, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int32_t H, int32_t stages, int32_t ncw)
+__host__ __device__ inline SmemLayout smem_layout(int32_t H, int32_t stages, int32_t rows, int32_t ncw)
 {
     SmemLayout L;
     L.row_stride = (static_cast<uint32_t>(H) * 2u + 127u) & ~127u;
-    L.bars = static_cast<uint32_t>(stages) * L.row_stride;
+    L.slot_stride = L.row_stride * static_cast<uint32_t>(rows);
+    L.bars = static_cast<uint32_t>(stages) * L.slot_stride;
     L.meta = L.bars + (2u * stages + 2u) * 8u;  // full[S], empty[S], reduction barrier, pad
     L.red = L.meta + static_cast<uint32_t>(stages) * static_cast<uint32_t>(sizeof(StageMeta));
     L.total = L.red + 2u * static_cast<uint32_t>(ncw) * 4u;
@@ -130,17 +143,19 @@ __device__ __forceinline__ int32_t ue8m0_byte(float amax)
 }
 
 template <int VPT, int QUANT>
-__global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) combine_kernel(const Params p)
+__global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combine_kernel(const Params p)
 {
+    constexpr int RMAX = max_rows<VPT>();
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ncw = (blockDim.x >> 5) - 1;
     const int NC = ncw * 32;
     const int S = p.stages;
+    const int R = p.rows;
     const int32_t H = p.H, k = p.k;
     const int32_t nvec = H >> 3;
     const uint32_t row_bytes = static_cast<uint32_t>(H) * 2u;
-    const SmemLayout L = smem_layout(H, S, ncw);
+    const SmemLayout L = smem_layout(H, S, R, ncw);
     const uint32_t ring = smem_u32(smem);
     const uint32_t full0 = ring + L.bars, empty0 = full0 + 8u * S, redbar = empty0 + 8u * S;
     StageMeta *meta = reinterpret_cast<StageMeta *>(smem + L.meta);
@@ -182,64 +197,78 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) combine_kerne
                 report(p.status, MOE_ERR_ROW_OUT_OF_RANGE);
                 valid = false;
             }
-            uint32_t m = __ballot_sync(0xffffffffu, valid);
-            const int n_items = __popc(m) + (p.shared ? 1 : 0) + (p.residual ? 1 : 0);
-            int item = 0;
-            // lane 0 fills the next ring slot with one row (src == nullptr: an
-            // empty marker); false if the slot never freed up
-            auto produce = [&](const uint8_t *src, float wt, int32_t flags) {
+            uint32_t mrem = __ballot_sync(0xffffffffu, valid);
+            const int n_exp = __popc(mrem);
+            const bool has_sh = p.shared != nullptr, has_res = p.residual != nullptr;
+            const int n = n_exp + (has_sh ? 1 : 0) + (has_res ? 1 : 0);
+            int i = 0;
+            do {  // one ring slot per iteration; a token with no rows still gets one
+                const int ns = (n - i < R) ? n - i : R;
+                const uint8_t *src[RMAX];
+                float wt[RMAX];
+#pragma unroll
+                for (int q = 0; q < RMAX; ++q) {
+                    src[q] = nullptr;
+                    wt[q] = 1.f;
+                    const int ii = i + q;
+                    if (q < ns) {  // warp-uniform
+                        if (ii < n_exp) {
+                            const int j = __ffs(mrem) - 1;
+                            mrem &= mrem - 1;
+                            const int32_t rj = __shfl_sync(0xffffffffu, r, j);
+                            wt[q] = __shfl_sync(0xffffffffu, w, j);
+                            src[q] = p.expert_out + static_cast<int64_t>(rj) * row_bytes;
+                        } else if (has_sh && ii == n_exp) {
+                            src[q] = p.shared + t * row_bytes;
+                        } else {
+                            src[q] = p.residual + t * row_bytes;
+                        }
+                    }
+                }
+                const bool last = (i + ns >= n);
                 bool good = true;
                 if (lane == 0) {
                     good = mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, kWaitLimitNs);
                     if (good) {
-                        meta[stage] = StageMeta{static_cast<int32_t>(t), wt, flags, 0};
-                        if (src) {
-                            mbar_arrive_expect_tx(full0 + 8u * stage, row_bytes);
-                            bulk_g2s(ring + static_cast<uint32_t>(stage) * L.row_stride, src, row_bytes,
-                                     full0 + 8u * stage);
+                        StageMeta &m = meta[stage];
+                        m.t = static_cast<int32_t>(t);
+                        m.n = ns;
+                        m.flags = (last ? F_LAST : 0) | ((last && has_res && ns > 0) ? F_RESID : 0);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            m.w[q] = q < RMAX ? wt[q < RMAX ? q : 0] : 1.f;
+                        const uint32_t full = full0 + 8u * stage;
+                        if (ns > 0) {
+                            mbar_arrive_expect_tx(full, static_cast<uint32_t>(ns) * row_bytes);
+                            const uint32_t dst = ring + static_cast<uint32_t>(stage) * L.slot_stride;
+#pragma unroll
+                            for (int q = 0; q < RMAX; ++q)
+                                if (q < ns)
+                                    bulk_g2s(dst + static_cast<uint32_t>(q) * L.row_stride, src[q], row_bytes, full);
                         } else {
-                            mbar_arrive(full0 + 8u * stage);
+                            mbar_arrive(full);
                         }
                     }
                 }
                 good = __shfl_sync(0xffffffffu, good, 0);
-                if (good) {
-                    ++issued;
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                if (!good) {
+                    ok = false;
+                    break;
                 }
-                return good;
-            };
-            if (n_items == 0) {
-                ok = produce(nullptr, 0.f, F_EMPTY | F_LAST);
-                continue;
-            }
-            while (m && ok) {
-                const int j = __ffs(m) - 1;
-                m &= m - 1;
-                const int32_t rj = __shfl_sync(0xffffffffu, r, j);
-                const float wj = __shfl_sync(0xffffffffu, w, j);
-                ++item;
-                ok = produce(p.expert_out + static_cast<int64_t>(rj) * row_bytes, wj,
-                             F_EXPERT | (item == n_items ? F_LAST : 0));
-            }
-            if (p.shared && ok) {
-                ++item;
-                ok = produce(p.shared + t * row_bytes, 1.f, F_SHARED | (item == n_items ? F_LAST : 0));
-            }
-            if (p.residual && ok) {
-                ++item;
-                ok = produce(p.residual + t * row_bytes, 1.f, F_RESIDUAL | F_LAST);
-            }
+                ++issued;
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                i += ns;
+            } while (i < n);
         }
         if (!ok && lane == 0) {
             // a slot never freed up: record it, then let every copy this warp
             // started land before the CTA's shared memory goes away
             report(p.status, MOE_ERR_DEVICE_TIMEOUT);
-            const int64_t n = issued < S ? issued : S;
-            for (int64_t s = 0; s < n; ++s) {
+            const int64_t nn = issued < S ? issued : S;
+            for (int64_t s = 0; s < nn; ++s) {
                 const int64_t times = (issued - 1 - s) / S + 1;
                 mbar_wait_bounded(full0 + 8u * static_cast<uint32_t>(s), static_cast<uint32_t>((times - 1) & 1),
                                   kWaitLimitNs);
@@ -252,13 +281,13 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) combine_kerne
     const int tid = threadIdx.x;
     // pad rows of a swizzled scale matrix are written as zero
     if (QUANT != MOE_QUANT_NONE && p.sf_layout == MOE_SF_SWIZZLED_128x4 && p.sf_rows_pad > p.T) {
-        const int64_t n = (p.sf_rows_pad - p.T) * p.sf_cols_pad;
-        for (int64_t i = static_cast<int64_t>(blockIdx.x) * NC + tid; i < n;
+        const int64_t nz = (p.sf_rows_pad - p.T) * p.sf_cols_pad;
+        for (int64_t i = static_cast<int64_t>(blockIdx.x) * NC + tid; i < nz;
              i += static_cast<int64_t>(gridDim.x) * NC)
             p.scales_out[sf_offset(p.T + i / p.sf_cols_pad, i % p.sf_cols_pad, p)] = 0;
     }
-
     const bool do_norm = p.gamma != nullptr;
+    const int max_slots = k + 3;  // a token never needs more slots than rows + 1
 
     int stage = 0;
     uint32_t phase = 0;
@@ -271,14 +300,28 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) combine_kerne
             for (int i = 0; i < 8; ++i)
                 acc[s][i] = 0.f;
         bool combined_done = false;
-        for (int it = 0; it < k + 3; ++it) {
+        for (int it = 0; it < max_slots; ++it) {
             if (!mbar_wait_bounded(full0 + 8u * stage, phase, kWaitLimitNs)) {
                 report(p.status, MOE_ERR_DEVICE_TIMEOUT);
                 return;
             }
             const StageMeta m = meta[stage];
-            if (!(m.flags & F_EMPTY)) {
-                if ((m.flags & F_RESIDUAL) && p.combined_out) {
+            const uint8_t *slot = smem + static_cast<uint32_t>(stage) * L.slot_stride;
+            uint4 q[RMAX][VPT];
+#pragma unroll
+            for (int rr = 0; rr < RMAX; ++rr)
+#pragma unroll
+                for (int s = 0; s < VPT; ++s) {
+                    const int v = s * NC + tid;
+                    q[rr][s] = make_uint4(0, 0, 0, 0);
+                    if (rr < m.n && v < nvec)
+                        q[rr][s] = *reinterpret_cast<const uint4 *>(slot + rr * L.row_stride + 16 * v);
+                }
+#pragma unroll
+            for (int rr = 0; rr < RMAX; ++rr) {
+                if (rr >= m.n)
+                    break;
+                if ((m.flags & F_RESID) && rr == m.n - 1 && p.combined_out) {
 #pragma unroll
                     for (int s = 0; s < VPT; ++s) {
                         const int v = s * NC + tid;
@@ -287,25 +330,18 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) combine_kerne
                     }
                     combined_done = true;
                 }
-                const uint8_t *row = smem + static_cast<uint32_t>(stage) * L.row_stride;
-                uint4 q[VPT];
-#pragma unroll
-                for (int s = 0; s < VPT; ++s) {
-                    const int v = s * NC + tid;
-                    if (v < nvec)
-                        q[s] = *reinterpret_cast<const uint4 *>(row + 16 * v);
-                }
+                const float wr = m.w[rr];
 #pragma unroll
                 for (int s = 0; s < VPT; ++s) {
                     const int v = s * NC + tid;
                     if (v < nvec) {
-                        const uint32_t qw[4] = {q[s].x, q[s].y, q[s].z, q[s].w};
+                        const uint32_t qw[4] = {q[rr][s].x, q[rr][s].y, q[rr][s].z, q[rr][s].w};
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             float lo, hi;
                             bf16x2_to_f32(qw[i], lo, hi);
-                            acc[s][2 * i] = fmaf(m.w, lo, acc[s][2 * i]);
-                            acc[s][2 * i + 1] = fmaf(m.w, hi, acc[s][2 * i + 1]);
+                            acc[s][2 * i] = fmaf(wr, lo, acc[s][2 * i]);
+                            acc[s][2 * i + 1] = fmaf(wr, hi, acc[s][2 * i + 1]);
                         }
                     }
                 }
@@ -459,49 +495,55 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1) combine_kerne
 
 // ------------------------------------------------------------------- host
 
+// Process-wide plan overrides set by moe_tuning_set (0 = automatic).
+struct Tuning {
+    int vpt = 0, rows = 0, ring_kib = 0, ctas_per_sm = 0;
+};
+Tuning g_tuning;
+
 struct Plan {
-    int vpt, ncw, stages, ctas_per_sm;
+    int vpt, ncw, rows, stages, ctas_per_sm;
     SmemLayout smem;
 };
 
-// Tuning knobs (environment, read once): NQG_COMBINE_CTAS_PER_SM (1..4,
-// default 1) splits the shared-memory budget between that many resident
-// CTAs per SM; NQG_COMBINE_STAGES caps the ring depth.
-int env_int(const char *name, int dflt, int lo, int hi)
-{
-    const char *v = std::getenv(name);
-    if (!v || !*v)
-        return dflt;
-    const int x = std::atoi(v);
-    return x < lo ? lo : (x > hi ? hi : x);
-}
-
-// Vectors per consumer thread: the smallest of 1, 2, 4, 8 that covers the
-// row with at most kMaxConsumerWarps consumer warps; ring depth: as many
-// whole rows as fit the shared-memory budget, 2..32.
+// Vectors per consumer thread: 2 where it covers the row (measured best on
+// GB300 at H = 7168: 14 consumer warps with 2 vectors each beat 7 x 4, which
+// is latency-bound, and 28 x 1, which pays per-row overhead), else 4, 8, 1.
+// Rows per ring slot: 2, or fewer where the registers allow fewer.  Ring:
+// about kDefaultRingBytes of rows, at least 2 slots, within the budget.
 Plan make_plan(int32_t H)
 {
-    static const int ctas_per_sm = env_int("NQG_COMBINE_CTAS_PER_SM", 1, 1, 4);
-    static const int max_stages = env_int("NQG_COMBINE_STAGES", kMaxStages, 2, kMaxStages);
+    const Tuning tu = g_tuning;
     Plan pl{};
     const int nvec = H / 8;
+    auto covers = [&](int v) { return (nvec + 32 * v - 1) / (32 * v) <= max_consumer_warps_rt(v); };
     pl.vpt = 8;
-    for (int v : {1, 2, 4, 8}) {
-        if ((nvec + 32 * v - 1) / (32 * v) <= kMaxConsumerWarps) {
-            pl.vpt = v;
-            break;
+    if (tu.vpt && covers(tu.vpt)) {
+        pl.vpt = tu.vpt;
+    } else {
+        for (int v : {2, 4, 8, 1}) {
+            if (covers(v)) {
+                pl.vpt = v;
+                break;
+            }
         }
     }
     pl.ncw = (nvec + 32 * pl.vpt - 1) / (32 * pl.vpt);
-    const SmemLayout one = smem_layout(H, 1, pl.ncw);
-    const size_t fixed = one.total - one.row_stride - 16 - sizeof(StageMeta);
-    const size_t per_stage = one.row_stride + 16 + sizeof(StageMeta);
+    const int rmax = max_rows_rt(pl.vpt);
+    pl.rows = tu.rows ? (tu.rows < rmax ? tu.rows : rmax) : (2 < rmax ? 2 : rmax);
+    pl.ctas_per_sm = tu.ctas_per_sm ? tu.ctas_per_sm : 1;
     // one CTA keeps kSmemBudget; several share the SM's 228 KB (1 KB reserved each)
-    const size_t budget = ctas_per_sm == 1 ? kSmemBudget : (224 * 1024) / ctas_per_sm - 2048;
-    const int s = static_cast<int>((budget - fixed) / per_stage);
-    pl.stages = s < 2 ? 2 : (s > max_stages ? max_stages : s);
-    pl.ctas_per_sm = ctas_per_sm;
-    pl.smem = smem_layout(H, pl.stages, pl.ncw);
+    const size_t budget = pl.ctas_per_sm == 1 ? kSmemBudget : (224 * 1024) / pl.ctas_per_sm - 2048;
+    const SmemLayout one = smem_layout(H, 1, pl.rows, pl.ncw);
+    const size_t per_slot = one.slot_stride + 16 + sizeof(StageMeta);
+    const size_t fixed = one.total - per_slot;
+    const size_t ring = tu.ring_kib ? static_cast<size_t>(tu.ring_kib) * 1024 : kDefaultRingBytes;
+    int s = static_cast<int>((ring + one.slot_stride / 2) / one.slot_stride);
+    const int fit = budget > fixed ? static_cast<int>((budget - fixed) / per_slot) : 0;
+    s = s > fit ? fit : s;
+    s = s > kMaxStages ? kMaxStages : s;
+    pl.stages = s < 2 ? 2 : s;
+    pl.smem = smem_layout(H, pl.stages, pl.rows, pl.ncw);
     return pl;
 }
 
@@ -514,6 +556,8 @@ moe_status launch_t(const Params &p, const Plan &pl, cudaStream_t stream)
     if (cudaGetDevice(&dev) != cudaSuccess)
         return MOE_ERR_CUDA;
     const int need = static_cast<int>(pl.smem.total);
+    if (need > 227 * 1024)
+        return MOE_ERR_UNSUPPORTED;
     if (dev < 0 || dev >= 64 || configured_for[dev] < need) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, need) != cudaSuccess)
             return MOE_ERR_CUDA;
@@ -543,6 +587,20 @@ moe_status launch_q(const Params &p, const Plan &pl, cudaStream_t stream)
 } // namespace nqg
 
 using namespace nqg;
+
+extern "C" moe_status moe_tuning_set(int32_t vpt, int32_t rows_per_slot, int32_t ring_kib, int32_t ctas_per_sm)
+{
+    if (!(vpt == 0 || vpt == 1 || vpt == 2 || vpt == 4 || vpt == 8))
+        return MOE_ERR_INVALID_ARG;
+    if (rows_per_slot < 0 || rows_per_slot > 4 || ring_kib < 0 || ring_kib > 224 || ctas_per_sm < 0 ||
+        ctas_per_sm > 4)
+        return MOE_ERR_INVALID_ARG;
+    g_tuning.vpt = vpt;
+    g_tuning.rows = rows_per_slot;
+    g_tuning.ring_kib = ring_kib;
+    g_tuning.ctas_per_sm = ctas_per_sm;
+    return MOE_OK;
+}
 
 extern "C" moe_status moe_combine(const moe_combine_args *a, moe_stream_t stream)
 {
@@ -616,6 +674,7 @@ extern "C" moe_status moe_combine(const moe_combine_args *a, moe_stream_t stream
     }
     const Plan pl = make_plan(a->H);
     p.stages = pl.stages;
+    p.rows = pl.rows;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (a->quant) {
     case MOE_QUANT_MXFP8: return launch_q<MOE_QUANT_MXFP8>(p, pl, s);

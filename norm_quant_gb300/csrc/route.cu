@@ -16,8 +16,8 @@
 // bit-exact: no atomics decide a position.  No kernel waits on another CTA.
 //
 // For N <= kFusedMaxSlots and E <= kFusedMaxExperts the three steps run as
-// ONE launch (route_fused_kernel): a thread-block cluster of up to 8 CTAs of
-// 32 warps, one chunk per warp.  Each CTA keeps its chunk histograms in
+// ONE launch (route_fused_kernel): a thread-block cluster of up to 16 CTAs
+// (8 where 16 cannot be placed) of 32 warps, one chunk per warp.  Each CTA keeps its chunk histograms in
 // shared memory; after a cluster barrier every CTA reads the per-expert
 // totals of the others through distributed shared memory, derives offsets
 // and its own chunk bases, and scatters.  Cluster barriers are hardware
@@ -237,29 +237,23 @@ __global__ void route_scatter_kernel(const int32_t *__restrict__ ids, int64_t N,
 
 constexpr int kFusedThreads = 1024;
 constexpr int kFusedWarps = kFusedThreads / 32;
-constexpr int kFusedMaxCtas = 8;                 // portable cluster size
-constexpr int kFusedMaxPerLane = 32;             // chunk <= 1024 slots
+constexpr int kFusedMaxCtas = 16;                // non-portable cluster size where allowed
+constexpr int kFusedMaxPerLane = 32;             // chunk <= 1024 slots per warp
 constexpr int64_t kFusedMaxSlots = int64_t(kFusedMaxCtas) * kFusedWarps * 32 * kFusedMaxPerLane;
 constexpr int kFusedMaxExperts = 1024;
+constexpr int kParts = 4;                        // the cross-warp prefix runs 4-way parallel
+constexpr int kTile = kFusedThreads / kParts;    // experts per prefix pass
 
 struct FusedPlan {
-    int ctas, chunk;  // chunk: slots per warp, a multiple of 32
+    int ctas, per_lane;  // cluster size; slots per lane (chunk = 32 * per_lane per warp)
     size_t smem;
 };
 
-FusedPlan fused_plan(int64_t N, int32_t E)
+size_t fused_smem(int32_t E)
 {
-    FusedPlan f{};
-    const int64_t per_cta_at_256 = int64_t(kFusedWarps) * 256;
-    int64_t ctas = (N + per_cta_at_256 - 1) / per_cta_at_256;
-    f.ctas = static_cast<int>(ctas < 1 ? 1 : (ctas > kFusedMaxCtas ? kFusedMaxCtas : ctas));
-    const int64_t warps = int64_t(f.ctas) * kFusedWarps;
-    f.chunk = static_cast<int>(((N + warps - 1) / warps + 31) / 32 * 32);
-    if (f.chunk < 32)
-        f.chunk = 32;
-    // hist[32][E] + tot[E] + cnt[E] + pre[E] + off[E + 1] + warp sums[32]
-    f.smem = (static_cast<size_t>(kFusedWarps) * E + 4 * static_cast<size_t>(E) + 1 + 32) * sizeof(int32_t);
-    return f;
+    // hist[32][E] + tot[E] + cnt[E] + pre[E] + off[E + 1] + psum[4][256] + wsum[32]
+    return (static_cast<size_t>(kFusedWarps) * E + 4 * static_cast<size_t>(E) + 1 + kParts * kTile + 32) *
+           sizeof(int32_t);
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -279,70 +273,106 @@ __device__ __forceinline__ void cluster_sync_all()
 __device__ __forceinline__ int32_t ld_dsmem(const int32_t *local, uint32_t rank)
 {
     uint32_t remote, v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+    asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
     return static_cast<int32_t>(v);
 }
 
+// One cluster of gridDim.x CTAs (the whole grid), 32 warps each; warp w of
+// CTA b owns the chunk of PL * 32 consecutive slots starting at
+// (b * 32 + w) * PL * 32.  Every thread reaches every barrier.
+template <int PL>
 __global__ void __launch_bounds__(kFusedThreads, 1)
-    route_fused_kernel(const int32_t *__restrict__ ids, int64_t N, int32_t E, int32_t chunk,
-                       int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
-                       int32_t *__restrict__ row_map, int32_t *__restrict__ src_row, int32_t *__restrict__ err)
+    route_fused_kernel(const int32_t *__restrict__ ids, int64_t N, int32_t E, int32_t *__restrict__ counts,
+                       int32_t *__restrict__ offsets, int32_t *__restrict__ row_map,
+                       int32_t *__restrict__ src_row, int32_t *__restrict__ err)
 {
     extern __shared__ int32_t sh[];
-    int32_t *hist = sh;                                     // [32][E]
+    int32_t *hist = sh;                                          // [32][E]
     int32_t *tot = hist + static_cast<size_t>(kFusedWarps) * E;  // [E] this CTA's totals (read remotely)
-    int32_t *cnt = tot + E;                                 // [E] cluster-wide counts
-    int32_t *pre = cnt + E;                                 // [E] counts of lower-ranked CTAs
-    int32_t *off = pre + E;                                 // [E + 1] offsets
-    int32_t *wsum = off + E + 1;                            // [32] scan scratch
+    int32_t *cnt = tot + E;                                      // [E] cluster-wide counts
+    int32_t *pre = cnt + E;                                      // [E] counts of lower-ranked CTAs
+    int32_t *off = pre + E;                                      // [E + 1] offsets
+    int32_t *psum = off + E + 1;                                 // [4][256] part sums
+    int32_t *wsum = psum + kParts * kTile;                       // [32] scan scratch
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
-    const uint32_t nctas = gridDim.x;  // the whole grid is one cluster
-    const int per_lane = chunk >> 5;
-    const int64_t first = (static_cast<int64_t>(rank) * kFusedWarps + warp) * chunk;
+    const int nctas = static_cast<int>(gridDim.x);
+    const int64_t first = (static_cast<int64_t>(rank) * kFusedWarps + warp) * (PL * 32);
+    const int part = threadIdx.x / kTile, el = threadIdx.x % kTile;
 
-    // 1. chunk histograms (every thread reaches every barrier below)
+    // 1. chunk histograms
     int32_t *h = hist + static_cast<size_t>(warp) * E;
     for (int e = lane; e < E; e += 32)
         h[e] = 0;
+    int32_t v[PL];
+#pragma unroll
+    for (int it = 0; it < PL; ++it) {
+        const int64_t i = first + it * 32 + lane;
+        v[it] = (i < N) ? __ldg(ids + i) : -1;
+    }
     __syncwarp();
-    int32_t v[kFusedMaxPerLane];
     bool bad = false;
 #pragma unroll
-    for (int it = 0; it < kFusedMaxPerLane; ++it) {
-        const int64_t i = first + it * 32 + lane;
-        v[it] = (it < per_lane && i < N) ? __ldg(ids + i) : -1;
-    }
-#pragma unroll
-    for (int it = 0; it < kFusedMaxPerLane; ++it) {
+    for (int it = 0; it < PL; ++it) {
         const int32_t e = v[it];
         if (e >= 0 && e < E)
             atomicAdd(&h[e], 1);
         else if (e != -1)
             bad = true;
     }
+    // the error word is cleared by CTA 0 before the first cluster barrier and
+    // only OR-ed into after it
+    if (rank == 0 && threadIdx.x == 0)
+        *err = 0;
+    __syncthreads();
+    // 2. exclusive prefix over this CTA's 32 warps per expert: part p of the
+    //    threads owns warps [8p, 8p + 8), then the parts combine in smem
+    for (int e0 = 0; e0 < E; e0 += kTile) {
+        const int e = e0 + el;
+        int32_t run = 0;
+        if (e < E) {
+#pragma unroll
+            for (int i = 0; i < kFusedWarps / kParts; ++i) {
+                int32_t *cell = &hist[static_cast<size_t>(part * (kFusedWarps / kParts) + i) * E + e];
+                const int32_t x = *cell;
+                *cell = run;
+                run += x;
+            }
+            psum[part * kTile + el] = run;
+        }
+        __syncthreads();
+        if (e < E) {
+            int32_t before = 0, all = 0;
+#pragma unroll
+            for (int q = 0; q < kParts; ++q) {
+                const int32_t x = psum[q * kTile + el];
+                before += (q < part) ? x : 0;
+                all += x;
+            }
+            if (before)
+#pragma unroll
+                for (int i = 0; i < kFusedWarps / kParts; ++i)
+                    hist[static_cast<size_t>(part * (kFusedWarps / kParts) + i) * E + e] += before;
+            if (part == 0)
+                tot[e] = all;
+        }
+        __syncthreads();
+    }
+    // 3. publish totals to the cluster; each CTA reads every CTA's totals
+    cluster_sync_all();
     if (__any_sync(0xffffffffu, bad) && lane == 0)
         atomicOr(err, 1);
-    __syncthreads();
-    // 2. per-expert exclusive prefix over this CTA's warps; CTA totals
     for (int e = threadIdx.x; e < E; e += kFusedThreads) {
-        int32_t run = 0;
-        for (int w = 0; w < kFusedWarps; ++w) {
-            const int32_t x = hist[static_cast<size_t>(w) * E + e];
-            hist[static_cast<size_t>(w) * E + e] = run;
-            run += x;
-        }
-        tot[e] = run;
-    }
-    // 3. publish totals to the cluster
-    cluster_sync_all();
-    for (int e = threadIdx.x; e < E; e += kFusedThreads) {
+        int32_t x[kFusedMaxCtas];
+#pragma unroll
+        for (int b = 0; b < kFusedMaxCtas; ++b)  // all remote reads in flight at once
+            x[b] = (b < nctas) ? ld_dsmem(tot + e, static_cast<uint32_t>(b)) : 0;
         int32_t all = 0, before = 0;
-        for (uint32_t b = 0; b < nctas; ++b) {
-            const int32_t x = (b == rank) ? tot[e] : ld_dsmem(tot + e, b);
-            all += x;
-            before += (b < rank) ? x : 0;
+#pragma unroll
+        for (int b = 0; b < kFusedMaxCtas; ++b) {
+            all += x[b];
+            before += (b < static_cast<int>(rank)) ? x[b] : 0;
         }
         cnt[e] = all;
         pre[e] = before;
@@ -353,9 +383,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     // 5. exclusive scan of cnt over experts (one contiguous range per thread)
     {
         const int per_t = (E + kFusedThreads - 1) / kFusedThreads;
-        const int e0 = threadIdx.x * per_t, e1 = (e0 + per_t < E) ? e0 + per_t : E;
+        const int ea = threadIdx.x * per_t, eb = (ea + per_t < E) ? ea + per_t : E;
         int32_t s = 0;
-        for (int e = e0; e < e1; ++e)
+        for (int e = ea; e < eb; ++e)
             s += cnt[e];
         int32_t incl = s;
 #pragma unroll
@@ -382,7 +412,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         }
         __syncthreads();
         int32_t run = wsum[warp] + incl - s;
-        for (int e = e0; e < e1; ++e) {
+        for (int e = ea; e < eb; ++e) {
             off[e] = run;
             run += cnt[e];
         }
@@ -396,18 +426,21 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         if (threadIdx.x == 0)
             offsets[E] = off[E];
     }
-    // 6. chunk bases
-    for (int idx = threadIdx.x; idx < kFusedWarps * E; idx += kFusedThreads) {
-        const int e = idx % E;
-        hist[idx] += off[e] + pre[e];
+    // 6. chunk bases: offsets + lower CTAs + lower warps of this CTA
+    for (int e0 = 0; e0 < E; e0 += kTile) {
+        const int e = e0 + el;
+        if (e < E) {
+            const int32_t base = off[e] + pre[e];
+#pragma unroll
+            for (int i = 0; i < kFusedWarps / kParts; ++i)
+                hist[static_cast<size_t>(part * (kFusedWarps / kParts) + i) * E + e] += base;
+        }
     }
     __syncthreads();
     // 7. stable scatter of this warp's chunk
     const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
-    for (int it = 0; it < kFusedMaxPerLane; ++it) {
-        if (it >= per_lane)
-            break;
+    for (int it = 0; it < PL; ++it) {
         const int64_t i = first + it * 32 + lane;
         const int32_t e = v[it];
         const bool valid = (e >= 0) && (e < E);
@@ -428,45 +461,85 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
 }
 
-// Whether one cluster of f.ctas CTAs with f.smem bytes of shared memory can
-// be placed on this device (cached per device, cluster size and smem size).
-bool fused_launchable(const FusedPlan &f)
+using FusedFn = void (*)(const int32_t *, int64_t, int32_t, int32_t *, int32_t *, int32_t *, int32_t *, int32_t *);
+
+FusedFn fused_fn(int per_lane)
 {
-    constexpr int kBuckets = 8;
-    static int cache[64][kFusedMaxCtas + 1][kBuckets];  // 0 unknown, 1 yes, 2 no
-    static bool attr_set[64];
+    switch (per_lane) {
+    case 1: return route_fused_kernel<1>;
+    case 2: return route_fused_kernel<2>;
+    case 4: return route_fused_kernel<4>;
+    case 8: return route_fused_kernel<8>;
+    case 16: return route_fused_kernel<16>;
+    default: return route_fused_kernel<32>;
+    }
+}
+
+// Whether one cluster of `ctas` CTAs with `smem` bytes can be placed on this
+// device; cached per device, kernel, cluster size and 32 KiB smem bucket.
+bool fused_fits(FusedFn fn, int per_lane, int ctas, size_t smem)
+{
+    static signed char cache[64][6][kFusedMaxCtas + 1][8];  // 0 unknown, 1 yes, -1 no
+    static bool attr_set[64][6];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return false;
-    const int bucket = static_cast<int>((f.smem + 32 * 1024 - 1) / (32 * 1024));  // <= 5 for E <= 1024
-    if (bucket >= kBuckets)
+    const int pl_idx = per_lane == 1 ? 0 : per_lane == 2 ? 1 : per_lane == 4 ? 2 : per_lane == 8 ? 3 : per_lane == 16 ? 4 : 5;
+    const int bucket = static_cast<int>((smem + 32 * 1024 - 1) / (32 * 1024));
+    if (bucket >= 8 || static_cast<size_t>(bucket) * 32 * 1024 > 227 * 1024)
         return false;
-    if (cache[dev][f.ctas][bucket])
-        return cache[dev][f.ctas][bucket] == 1;
-    if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(route_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kBuckets * 32 * 1024 - 1024) != cudaSuccess) {
+    signed char &c = cache[dev][pl_idx][ctas][bucket];
+    if (c)
+        return c > 0;
+    if (!attr_set[dev][pl_idx]) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess ||
+            cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
             cudaGetLastError();
             return false;
         }
-        attr_set[dev] = true;
+        attr_set[dev][pl_idx] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = f.ctas;
+    attr[0].val.clusterDim.x = ctas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(f.ctas);
+    cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(kFusedThreads);
     cfg.dynamicSmemBytes = static_cast<size_t>(bucket) * 32 * 1024;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    const bool ok = cudaOccupancyMaxActiveClusters(&n, route_fused_kernel, &cfg) == cudaSuccess && n > 0;
+    const bool ok = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void *>(fn), &cfg) == cudaSuccess && n > 0;
     cudaGetLastError();
-    cache[dev][f.ctas][bucket] = ok ? 1 : 2;
+    c = ok ? 1 : -1;
     return ok;
+}
+
+// Cluster size and slots per lane: enough CTAs that each holds at most
+// 32 * 32 * per_lane slots with the fewest slots per lane, preferring 16 CTAs
+// (or 8 where 16 cannot be placed); per_lane a power of two up to 32.
+bool fused_plan(int64_t N, int32_t E, FusedPlan *out)
+{
+    if (N > kFusedMaxSlots || E > kFusedMaxExperts)
+        return false;
+    const size_t smem = fused_smem(E);
+    for (int max_ctas : {16, 8}) {
+        const int64_t per_cta_min = int64_t(kFusedWarps) * 32;  // one slot per lane
+        int ctas = static_cast<int>((N + per_cta_min - 1) / per_cta_min);
+        ctas = ctas < 1 ? 1 : (ctas > max_ctas ? max_ctas : ctas);
+        int per_lane = 1;
+        while (int64_t(ctas) * kFusedWarps * 32 * per_lane < N)
+            per_lane *= 2;
+        if (per_lane > kFusedMaxPerLane)
+            continue;
+        if (fused_fits(fused_fn(per_lane), per_lane, ctas, smem)) {
+            *out = FusedPlan{ctas, per_lane, smem};
+            return true;
+        }
+    }
+    return false;
 }
 } // namespace
 } // namespace nqg
@@ -510,37 +583,36 @@ extern "C" moe_status moe_build_row_map(const int32_t *topk_ids, int64_t T, int3
     char *ws = static_cast<char *>(workspace);
     int32_t *err = reinterpret_cast<int32_t *>(ws + L.err_off);
     int32_t *hist = reinterpret_cast<int32_t *>(ws + L.hist_off);
-    if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess)
-        return MOE_ERR_CUDA;
     if (N == 0) {
-        if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s) != cudaSuccess ||
+        if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess ||
+            cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s) != cudaSuccess ||
             cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess)
             return MOE_ERR_CUDA;
         return MOE_OK;
     }
-    if (N <= kFusedMaxSlots && E <= kFusedMaxExperts) {
-        const FusedPlan f = fused_plan(N, E);
-        if (fused_launchable(f)) {
-            cudaLaunchConfig_t cfg = {};
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = f.ctas;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3(f.ctas);
-            cfg.blockDim = dim3(kFusedThreads);
-            cfg.dynamicSmemBytes = f.smem;
-            cfg.stream = s;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            if (cudaLaunchKernelEx(&cfg, route_fused_kernel, topk_ids, N, E, f.chunk, counts, offsets, row_map,
-                                   src_row, err) != cudaSuccess) {
-                cudaGetLastError();
-                return MOE_ERR_CUDA;
-            }
-            return MOE_OK;
+    FusedPlan f;
+    if (fused_plan(N, E, &f)) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = f.ctas;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(f.ctas);
+        cfg.blockDim = dim3(kFusedThreads);
+        cfg.dynamicSmemBytes = f.smem;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, fused_fn(f.per_lane), topk_ids, N, E, counts, offsets, row_map, src_row,
+                               err) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
         }
+        return MOE_OK;
     }
+    if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess)
+        return MOE_ERR_CUDA;
     const int wpc = warps_per_cta(E);
     const int grid = static_cast<int>((L.chunks + wpc - 1) / wpc);
     const size_t sh = static_cast<size_t>(wpc) * E * sizeof(int32_t);

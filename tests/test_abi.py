@@ -88,6 +88,15 @@ def test_combine_validation(L, kw, want):
     assert L.moe_combine(C.byref(a), None) == want
 
 
+def test_tuning_validation(L):
+    assert L.moe_tuning_set(3, 0, 0, 0) == 1
+    assert L.moe_tuning_set(0, 5, 0, 0) == 1
+    assert L.moe_tuning_set(0, 0, 300, 0) == 1
+    assert L.moe_tuning_set(0, 0, 0, 9) == 1
+    assert L.moe_tuning_set(2, 2, 144, 1) == 0
+    assert L.moe_tuning_set(0, 0, 0, 0) == 0
+
+
 def test_combine_null_args(L):
     assert L.moe_combine(None, None) == 1
 

@@ -146,7 +146,8 @@ def test_routing_sizes_and_determinism():
     rng = np.random.Generator(np.random.PCG64(6))
     # single-launch cluster path and (E > 1024 or N > 262144) the three-kernel path
     for T, k, E in [(1, 1, 1), (3, 2, 8192), (1000, 32, 5), (5000, 8, 1024), (70000, 2, 3),
-                    (40000, 8, 256), (33000, 8, 16), (2000, 8, 2048), (32768, 8, 256)]:
+                    (40000, 8, 256), (33000, 8, 16), (2000, 8, 2048), (32768, 8, 256),
+                    (16384, 8, 256), (70000, 8, 64)]:
         ids = rng.integers(-1, E, (T, k)).astype(np.int32)
         a = route_and_check(ids, E)[0]
         b = gpu_route(ids, E)[3]
@@ -199,3 +200,18 @@ def test_repeat_runs_identical_and_side_stream():
         b = gpu_combine(wl, inp, d_rm2, stream=s)
     for key in ("residual", "quant", "scales"):
         assert np.array_equal(a[key], b[key])
+
+
+@pytest.mark.parametrize("plan", [(1, 1, 0, 0), (1, 4, 0, 0), (2, 1, 0, 0), (2, 4, 32, 0), (4, 1, 0, 0),
+                                  (4, 2, 200, 0), (8, 1, 0, 0), (2, 2, 64, 2), (2, 2, 16, 3)],
+                         ids=lambda p: "vpt%d_rows%d_ring%d_cta%d" % p)
+def test_every_launch_plan_matches_the_oracle(plan):
+    """moe_tuning_set changes only how the work is laid out on the GPU."""
+    cases = [dataclasses.replace(synth.PREFILL, T=300, name="plan_mxfp8"),
+             dataclasses.replace(synth.GEMMA_NVFP4, T=257, name="plan_nvfp4")]
+    try:
+        nqg.moe_tuning_set(*plan)
+        for wl in cases:
+            run_workload(wl, canary=True)
+    finally:
+        nqg.moe_tuning_set(0, 0, 0, 0)
