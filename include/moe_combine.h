@@ -197,11 +197,15 @@ moe_status moe_combine(const moe_combine_args *args, moe_stream_t stream);
  *   rows_per_slot  rows staged per ring slot, 1..4 (capped at 4 for vpt <= 2,
  *                  2 for vpt 4, 1 for vpt 8);
  *   ring_kib       shared-memory ring size in KiB, 1..224 (capped to what fits);
- *   ctas_per_sm    resident CTAs per SM the grid is sized for, 1..4.
+ *   ctas_per_sm    resident CTAs per SM the grid is sized for, 1..4;
+ *   route_cluster  routing build: 0 automatic, -1 the three-kernel path,
+ *                  1..16 the largest thread-block cluster its single-launch
+ *                  path may use.
  * Not synchronised with calls in flight on other host threads.  Returns
  * MOE_OK or MOE_ERR_INVALID_ARG.  (No counterpart on the pages: a tuning
  * hook of this implementation.) */
-moe_status moe_tuning_set(int32_t vpt, int32_t rows_per_slot, int32_t ring_kib, int32_t ctas_per_sm);
+moe_status moe_tuning_set(int32_t vpt, int32_t rows_per_slot, int32_t ring_kib, int32_t ctas_per_sm,
+                          int32_t route_cluster);
 
 /* Bytes of the scale matrix for T rows of H elements: linear T * C, swizzled
  * roundup(T, 128) * roundup(C, 4), with C = H / 32 (MXFP8) or H / 16 (NVFP4). */

@@ -67,7 +67,7 @@ SYMBOLS = {
     "moe_combine": (C.c_int, [C.POINTER(MoeCombineArgs), C.c_void_p]),
     "moe_scales_bytes": (C.c_int, [C.c_int64, C.c_int32, C.c_int32, C.c_int32,
                                    C.POINTER(C.c_size_t)]),
-    "moe_tuning_set": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
+    "moe_tuning_set": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
 }
 
 
@@ -153,10 +153,10 @@ def moe_scales_bytes(T: int, H: int, quant: str, sf_layout: str = "linear") -> i
     return n.value
 
 
-def moe_tuning_set(vpt: int = 0, rows_per_slot: int = 0, ring_kib: int = 0, ctas_per_sm: int = 0) -> None:
-    """Overrides the combine kernel's launch plan (0 = automatic); results
-    do not depend on it."""
-    _check(lib().moe_tuning_set(vpt, rows_per_slot, ring_kib, ctas_per_sm), "moe_tuning_set")
+def moe_tuning_set(vpt: int = 0, rows_per_slot: int = 0, ring_kib: int = 0, ctas_per_sm: int = 0,
+                   route_cluster: int = 0) -> None:
+    """Overrides the launch plans (0 = automatic); results do not depend on it."""
+    _check(lib().moe_tuning_set(vpt, rows_per_slot, ring_kib, ctas_per_sm, route_cluster), "moe_tuning_set")
 
 
 def combine_args(*, expert_out, row_map, router_weights, shared_out=None, residual=None,

@@ -506,11 +506,13 @@ struct Plan {
     SmemLayout smem;
 };
 
-// Vectors per consumer thread: 2 where it covers the row (measured best on
-// GB300 at H = 7168: 14 consumer warps with 2 vectors each beat 7 x 4, which
-// is latency-bound, and 28 x 1, which pays per-row overhead), else 4, 8, 1.
-// Rows per ring slot: 2, or fewer where the registers allow fewer.  Ring:
-// about kDefaultRingBytes of rows, at least 2 slots, within the budget.
+// Vectors per consumer thread: the smallest of 1, 2, 4, 8 that needs at most
+// 16 consumer warps.  Rows per ring slot: as many as the registers allow (4
+// for VPT <= 2).  Measured on GB300: at H = 7168, 14 warps x 2 vectors with 4
+// rows per slot reach 93 % of HBM copy bandwidth, against 73 % for 7 warps x 4
+// (latency-bound) and 80 % for 28 warps x 1 (per-row overhead); at H = 4096,
+// 16 warps x 1 beat 8 x 2.  Ring: about kDefaultRingBytes of rows, at least 2
+// slots, within the shared-memory budget.
 Plan make_plan(int32_t H)
 {
     const Tuning tu = g_tuning;
@@ -521,8 +523,8 @@ Plan make_plan(int32_t H)
     if (tu.vpt && covers(tu.vpt)) {
         pl.vpt = tu.vpt;
     } else {
-        for (int v : {2, 4, 8, 1}) {
-            if (covers(v)) {
+        for (int v : {1, 2, 4, 8}) {
+            if (covers(v) && (nvec + 32 * v - 1) / (32 * v) <= 16) {
                 pl.vpt = v;
                 break;
             }
@@ -530,7 +532,7 @@ Plan make_plan(int32_t H)
     }
     pl.ncw = (nvec + 32 * pl.vpt - 1) / (32 * pl.vpt);
     const int rmax = max_rows_rt(pl.vpt);
-    pl.rows = tu.rows ? (tu.rows < rmax ? tu.rows : rmax) : (2 < rmax ? 2 : rmax);
+    pl.rows = tu.rows ? (tu.rows < rmax ? tu.rows : rmax) : rmax;
     pl.ctas_per_sm = tu.ctas_per_sm ? tu.ctas_per_sm : 1;
     // one CTA keeps kSmemBudget; several share the SM's 228 KB (1 KB reserved each)
     const size_t budget = pl.ctas_per_sm == 1 ? kSmemBudget : (224 * 1024) / pl.ctas_per_sm - 2048;
@@ -588,8 +590,12 @@ moe_status launch_q(const Params &p, const Plan &pl, cudaStream_t stream)
 
 using namespace nqg;
 
-extern "C" moe_status moe_tuning_set(int32_t vpt, int32_t rows_per_slot, int32_t ring_kib, int32_t ctas_per_sm)
+extern "C" moe_status moe_tuning_set(int32_t vpt, int32_t rows_per_slot, int32_t ring_kib, int32_t ctas_per_sm,
+                                     int32_t route_cluster)
 {
+    if (route_cluster < -1 || route_cluster > 16)
+        return MOE_ERR_INVALID_ARG;
+    nqg::set_route_cluster(route_cluster);
     if (!(vpt == 0 || vpt == 1 || vpt == 2 || vpt == 4 || vpt == 8))
         return MOE_ERR_INVALID_ARG;
     if (rows_per_slot < 0 || rows_per_slot > 4 || ring_kib < 0 || ring_kib > 224 || ctas_per_sm < 0 ||

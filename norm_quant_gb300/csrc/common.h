@@ -13,6 +13,10 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
+// Routing-build override from moe_tuning_set: 0 automatic, -1 the
+// three-kernel path, 1..16 the largest cluster the single-launch path may use.
+void set_route_cluster(int v);
+
 // Status of the launches just made: MOE_ERR_CUDA if any failed.
 inline moe_status launch_status()
 {

@@ -235,6 +235,8 @@ __global__ void route_scatter_kernel(const int32_t *__restrict__ ids, int64_t N,
 }
 
 
+int g_route_cluster = 0;  // see set_route_cluster
+
 constexpr int kFusedThreads = 1024;
 constexpr int kFusedWarps = kFusedThreads / 32;
 constexpr int kFusedMaxCtas = 16;                // non-portable cluster size where allowed
@@ -522,10 +524,12 @@ bool fused_fits(FusedFn fn, int per_lane, int ctas, size_t smem)
 // (or 8 where 16 cannot be placed); per_lane a power of two up to 32.
 bool fused_plan(int64_t N, int32_t E, FusedPlan *out)
 {
-    if (N > kFusedMaxSlots || E > kFusedMaxExperts)
+    if (N > kFusedMaxSlots || E > kFusedMaxExperts || g_route_cluster < 0)
         return false;
     const size_t smem = fused_smem(E);
     for (int max_ctas : {16, 8}) {
+        if (g_route_cluster > 0 && max_ctas > g_route_cluster)
+            max_ctas = g_route_cluster;
         const int64_t per_cta_min = int64_t(kFusedWarps) * 32;  // one slot per lane
         int ctas = static_cast<int>((N + per_cta_min - 1) / per_cta_min);
         ctas = ctas < 1 ? 1 : (ctas > max_ctas ? max_ctas : ctas);
@@ -542,6 +546,9 @@ bool fused_plan(int64_t N, int32_t E, FusedPlan *out)
     return false;
 }
 } // namespace
+
+void set_route_cluster(int v) { g_route_cluster = v; }
+
 } // namespace nqg
 
 using namespace nqg;

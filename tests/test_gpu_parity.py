@@ -142,7 +142,16 @@ def test_duplicate_experts_in_a_token():
     route_and_check(ids, 4)
 
 
-def test_routing_sizes_and_determinism():
+@pytest.mark.parametrize("cluster", [0, -1, 1, 4, 8])
+def test_routing_paths_and_determinism(cluster):
+    nqg.moe_tuning_set(route_cluster=cluster)
+    try:
+        _routing_sizes()
+    finally:
+        nqg.moe_tuning_set()
+
+
+def _routing_sizes():
     rng = np.random.Generator(np.random.PCG64(6))
     # single-launch cluster path and (E > 1024 or N > 262144) the three-kernel path
     for T, k, E in [(1, 1, 1), (3, 2, 8192), (1000, 32, 5), (5000, 8, 1024), (70000, 2, 3),
@@ -214,4 +223,4 @@ def test_every_launch_plan_matches_the_oracle(plan):
         for wl in cases:
             run_workload(wl, canary=True)
     finally:
-        nqg.moe_tuning_set(0, 0, 0, 0)
+        nqg.moe_tuning_set()
