@@ -13,7 +13,7 @@
 //   MXFP8: per 32 elements, e = smallest integer with amax <= 448 * 2^e,
 //          byte = clamp(e + 127, 0, 254), code = e4m3_rn_sat(y * 2^-e)
 //   NVFP4: v = g * y; per 16 elements s = e4m3_rn_sat(amax(v) / 6),
-//          code = e2m1_rn_sat(v / s) (0 when s == 0)
+//          code = e2m1_rn_sat(v * rn(1 / s)) (0 when s == 0)
 //
 // Design (an HBM-bound gather; no tensor cores -- nothing here is a
 // contraction):
@@ -340,8 +340,7 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                         for (int i = 0; i < 4; ++i) {
                             float lo, hi;
                             bf16x2_to_f32(qw[i], lo, hi);
-                            acc[s][2 * i] = fmaf(wr, lo, acc[s][2 * i]);
-                            acc[s][2 * i + 1] = fmaf(wr, hi, acc[s][2 * i + 1]);
+                            fma2(acc[s][2 * i], acc[s][2 * i + 1], lo, hi, wr);
                         }
                     }
                 }
@@ -473,10 +472,13 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                 if (vv) {
                     uint32_t packed = 0;
                     if (sf != 0.f) {
+                        // elements are scaled by the block scale's correctly
+                        // rounded fp32 reciprocal
+                        const float rs = __frcp_rn(sf);
                         float qv[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            qv[i] = __fdiv_rn(g[i], sf);
+                            qv[i] = g[i] * rs;
                         packed = cvt_e2m1x8(qv);
                     }
                     *reinterpret_cast<uint32_t *>(p.quant_out + (row0 >> 1) + 4 * v) = packed;

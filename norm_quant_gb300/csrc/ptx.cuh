@@ -135,6 +135,18 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float &lo, float &hi)
     hi = __uint_as_float(w & 0xFFFF0000u);
 }
 
+// acc = w * x + acc on two fp32 lanes at once (packed FMA, each lane rounded
+// to nearest exactly like fmaf).
+__device__ __forceinline__ void fma2(float &acc_lo, float &acc_hi, float x_lo, float x_hi, float w)
+{
+    uint64_t a, x, ww;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(acc_lo), "f"(acc_hi));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x_lo), "f"(x_hi));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(ww) : "f"(w));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(x), "l"(ww));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(acc_lo), "=f"(acc_hi) : "l"(a));
+}
+
 // Two fp32 -> bf16x2, round to nearest even; `lo` in the low half.
 __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi)
 {
