@@ -51,11 +51,11 @@ constexpr size_t kDefaultRingBytes = 144 * 1024;
 // consumer thread); the CTA adds one producer warp.  Together they cover
 // H <= 7168 (VPT 1), 8192 (VPT 2, 4) and 16384 (VPT 8).
 template <int VPT>
-constexpr int max_consumer_warps() { return VPT == 1 ? 28 : (VPT == 2 ? 16 : 8); }
+__host__ __device__ constexpr int max_consumer_warps() { return VPT == 1 ? 28 : (VPT == 2 ? 16 : 8); }
 inline int max_consumer_warps_rt(int vpt) { return vpt == 1 ? 28 : (vpt == 2 ? 16 : 8); }
 // Rows a ring slot may hold, bounded by the registers the loads take.
 template <int VPT>
-constexpr int max_rows() { return VPT <= 2 ? 4 : (VPT == 4 ? 2 : 1); }
+__host__ __device__ constexpr int max_rows() { return VPT <= 2 ? 4 : (VPT == 4 ? 2 : 1); }
 inline int max_rows_rt(int vpt) { return vpt <= 2 ? 4 : (vpt == 4 ? 2 : 1); }
 
 enum : int32_t { F_LAST = 1, F_RESID = 2 };
