@@ -140,6 +140,41 @@ moe_status moe_build_row_map(const int32_t *topk_ids, int64_t T, int32_t top_k, 
 moe_status moe_build_row_map_check(const void *workspace, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Routing build without a workspace (no counterpart on the pages: an
+ * addition of this library for callers that cannot allocate).
+ *
+ * Some callers cannot hand the library a workspace: plug-ins or extensions
+ * running inside a host framework that owns all device memory through its
+ * own allocator and offers them none, or latency-critical loops that may not
+ * call cudaMalloc / cudaFree, because those calls can synchronise the device
+ * or fail under memory pressure.  This entry point computes exactly what
+ * moe_build_row_map computes (same outputs, bit for bit) but keeps its
+ * scratch in a fixed array of MOE_NOALLOC_SCRATCH_BYTES bytes that the
+ * library holds on every GPU where it is loaded, until the process exits.
+ * It allocates nothing and calls no allocating routine.
+ *
+ *  - Limit: moe_build_row_map_workspace_size(T, top_k, E) must not exceed
+ *    MOE_NOALLOC_SCRATCH_BYTES (1 MiB: for example T * top_k up to about one
+ *    million slots with E = 256); larger problems return MOE_ERR_UNSUPPORTED.
+ *  - The first call on each device looks up the array's device address
+ *    (once per device, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the one array, and it keeps whatever the
+ *    last call left in it; every call rewrites the parts it reads.  Calls
+ *    that may overlap on the GPU (different streams, or host threads) race
+ *    on the array and must be serialised by the caller.
+ *  - error_flag: device int32 or NULL.  When given it receives 0, or a
+ *    nonzero value if an id outside [-1, E) was met (such ids are treated as
+ *    padding, as in moe_build_row_map).
+ * Other arguments, validation and return values as for moe_build_row_map.
+ * ---------------------------------------------------------------------- */
+#define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+moe_status moe_build_row_map_noalloc(const int32_t *topk_ids, int64_t T, int32_t top_k, int32_t E,
+                                     int32_t *counts, int32_t *offsets, int32_t *row_map,
+                                     int32_t *src_row, int32_t *error_flag, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Combine + residual + RMSNorm + quantisation, one call.
  * ---------------------------------------------------------------------- */
 typedef struct moe_combine_args {

@@ -64,6 +64,8 @@ SYMBOLS = {
                                     C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t,
                                     C.c_void_p]),
     "moe_build_row_map_check": (C.c_int, [C.c_void_p, C.c_void_p]),
+    "moe_build_row_map_noalloc": (C.c_int, [C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_void_p,
+                                            C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     "moe_combine": (C.c_int, [C.POINTER(MoeCombineArgs), C.c_void_p]),
     "moe_scales_bytes": (C.c_int, [C.c_int64, C.c_int32, C.c_int32, C.c_int32,
                                    C.POINTER(C.c_size_t)]),
@@ -140,6 +142,17 @@ def moe_build_row_map(topk_ids, E: int, counts, offsets, row_map, src_row=None,
                                    workspace.numel() * workspace.element_size() if workspace is not None else 0,
                                    _stream(stream)),
            "moe_build_row_map")
+
+
+def moe_build_row_map_noalloc(topk_ids, E: int, counts, offsets, row_map, src_row=None,
+                              error_flag=None, stream=None) -> None:
+    """moe_build_row_map without a workspace, for callers that cannot
+    allocate device memory: the library's own fixed scratch array is used
+    (see include/moe_combine.h for its size limit and sharing rules)."""
+    T, k = topk_ids.shape
+    _check(lib().moe_build_row_map_noalloc(_ptr(topk_ids), T, k, E, _ptr(counts), _ptr(offsets),
+                                           _ptr(row_map), _ptr(src_row), _ptr(error_flag), _stream(stream)),
+           "moe_build_row_map_noalloc")
 
 
 def moe_build_row_map_check(workspace, stream=None) -> int:
