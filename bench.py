@@ -61,6 +61,22 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest of every rank's x (x itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_rank: int, steps: int, max_seconds: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / max_seconds
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -341,10 +357,7 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
         comb_s = replay(g_comb, K) / K         # the combine kernel alone, same count
-    if world > 1:
-        t = torch.tensor([total_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s = max_over_ranks(total_s, dev)
 
     # end to end through the C ABI from pinned host buffers
     host_out = {n: torch.empty_like(t, device="cpu").pin_memory() for n, t in outs.items()}
@@ -367,11 +380,7 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_s = e0.elapsed_time(e1) / 1e3
-    if world > 1:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
 
     if rank == 0:
         byt = algorithmic_bytes(wl, inp["n_valid"])
@@ -379,7 +388,7 @@ def run_ours(args):
         achieved = byt["total"] / comb_avg_s / 1e9
         peak, peak_kind = measured_peak()
         line = {
-            "metric": METRIC, "value": world * T * K / total_s, "unit": "tokens/s", "n_gpus": world,
+            "metric": METRIC, "value": job_throughput(world, T, K, total_s), "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": total_s / K * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
@@ -397,7 +406,7 @@ def run_ours(args):
                          "frac": achieved / peak, "peak_source": peak_kind,
                          "kernel": "combine_kernel", "kernel_ms": comb_avg_s * 1e3,
                          "algorithmic_bytes": byt["total"], "traffic": recorded_traffic()},
-            "e2e": {"value": world * T * args.e2e_steps / e2e_s, "unit": "tokens/s",
+            "e2e": {"value": job_throughput(world, T, args.e2e_steps, e2e_s), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": (route_kernels + 1) * K,
             "clocks": clk.summary(),
