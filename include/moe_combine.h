@@ -56,7 +56,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 /* Limits of this implementation (validated on the host). */
 #define MOE_MAX_TOP_K 32
@@ -83,6 +83,17 @@ typedef enum {
     MOE_QUANT_NVFP4 = 2  /* e2m1 codes [T, H/2] bytes (element 2i in the low nibble)
                             + e4m3 scale per 16 elements, with global scale g */
 } moe_quant_kind;
+
+typedef enum {
+    MOE_LAYOUT_GROUPED = 0,    /* expert_out rows grouped by expert; row_map[t, j] gives
+                                  the row of (token t, slot j), -1 = padded slot */
+    MOE_LAYOUT_SLOT_MAJOR = 1  /* expert_out is [top_k, T, H]: slot j of token t is row
+                                  j * T + t, every slot present, row_map unused
+                                  (trtllm_moe_allreduce_fusion --
+                                  moe_reduction_active_experts_token_input, with
+                                  moe_reduction_scale_input as router_weights and
+                                  moe_reduction_token_input as shared_out) */
+} moe_expert_layout;
 
 typedef enum {
     MOE_SF_LINEAR = 0,         /* scale (row r, column c) at byte r*C + c */
@@ -181,9 +192,12 @@ typedef struct moe_combine_args {
     int64_t T;                    /* tokens (rows of every [T, *] tensor); 0 = no-op */
     int32_t H;                    /* hidden size; multiple of 8, <= MOE_MAX_HIDDEN */
     int32_t top_k;                /* slots per token, 1..MOE_MAX_TOP_K */
-    const void *expert_out;       /* device bf16 [n_expert_rows, H], grouped by expert */
-    int64_t n_expert_rows;        /* rows in expert_out (row_map entries must be below) */
-    const int32_t *row_map;       /* device int32 [T, top_k], -1 = padded slot */
+    const void *expert_out;       /* device bf16 [n_expert_rows, H]: grouped by expert,
+                                     or [top_k, T, H] slot-major (see expert_layout) */
+    int64_t n_expert_rows;        /* rows in expert_out (row_map entries must be below;
+                                     exactly top_k * T for the slot-major layout) */
+    const int32_t *row_map;       /* device int32 [T, top_k], -1 = padded slot; unused
+                                     (may be NULL) for the slot-major layout */
     const float *router_weights;  /* device fp32 [T, top_k], used as given */
     const void *shared_out;       /* device bf16 [T, H] or NULL: shared-expert row, weight 1 */
     const void *residual;         /* device bf16 [T, H] or NULL */
@@ -193,7 +207,7 @@ typedef struct moe_combine_args {
     int32_t quant;                /* moe_quant_kind */
     int32_t sf_layout;            /* moe_sf_layout (ignored when quant == NONE) */
     float global_scale;           /* NVFP4 g > 0: codes encode g * y (ignored otherwise) */
-    int32_t reserved0;            /* must be 0 */
+    int32_t expert_layout;        /* moe_expert_layout */
     void *combined_out;           /* device bf16 [T, H] or NULL: bf16(s) */
     void *residual_out;           /* device bf16 [T, H] or NULL: bf16(x) */
     void *norm_out;               /* device bf16 [T, H] or NULL: bf16(y); needs gamma */
@@ -211,9 +225,11 @@ typedef struct moe_combine_args {
  * the quantiser reads x directly.  Without residual, x = s.
  * Padded tokens (all slots -1) are still written: s = shared (or 0).
  * Host-side validation, before any launch:
- *   args non-NULL; T >= 0; reserved0 == 0; H % 8 == 0 and 8 <= H <= MOE_MAX_HIDDEN;
- *   1 <= top_k <= MOE_MAX_TOP_K; T == 0 then returns MOE_OK without looking at
- *   any pointer (empty tensors may carry NULL); otherwise row_map, router_weights non-NULL;
+ *   args non-NULL; T >= 0; expert_layout in {GROUPED, SLOT_MAJOR};
+ *   H % 8 == 0 and 8 <= H <= MOE_MAX_HIDDEN; 1 <= top_k <= MOE_MAX_TOP_K;
+ *   T == 0 then returns MOE_OK without looking at any pointer (empty tensors
+ *   may carry NULL); otherwise router_weights non-NULL; row_map non-NULL for
+ *   the grouped layout; n_expert_rows == top_k * T < 2^31 for the slot-major one;
  *   expert_out non-NULL when n_expert_rows > 0; every bf16 / byte tensor
  *   pointer 16-byte aligned; at least one output requested;
  *   norm_out needs gamma; quant in {NONE, MXFP8, NVFP4}; MXFP8 needs
@@ -241,6 +257,23 @@ moe_status moe_combine(const moe_combine_args *args, moe_stream_t stream);
  * hook of this implementation.) */
 moe_status moe_tuning_set(int32_t vpt, int32_t rows_per_slot, int32_t ring_kib, int32_t ctas_per_sm,
                           int32_t route_cluster);
+
+/* ------------------------------------------------------------------------
+ * Dispatch-side permute: the step before the expert computation, the
+ * inverse of the combine's gather (flashinfer.comm.moe_a2a_combine: combine
+ * is the inverse of moe_a2a_dispatch; Struct_ep_combine_skip_a2a: src_info).
+ *
+ * Copies token t's row x[t] (device bf16 [T, H]) to every row row_map[t, j]
+ * >= 0 of x_grouped (device bf16 [n_rows, H]), so that x_grouped holds the
+ * tokens grouped by expert in the order moe_build_row_map defines.  Rows no
+ * slot names are not written.  H % 8 == 0, 8 <= H <= MOE_MAX_HIDDEN,
+ * 1 <= top_k <= MOE_MAX_TOP_K; x and x_grouped 16-byte aligned.  A row_map
+ * entry >= n_rows is skipped and reported in *status (device int32 or NULL,
+ * zeroed by the caller) as MOE_ERR_ROW_OUT_OF_RANGE.  T == 0 is a no-op.
+ * ---------------------------------------------------------------------- */
+moe_status moe_dispatch_permute(const void *x, int64_t T, int32_t H, const int32_t *row_map,
+                                int32_t top_k, void *x_grouped, int64_t n_rows, int32_t *status,
+                                moe_stream_t stream);
 
 /* Bytes of the scale matrix for T rows of H elements: linear T * C, swizzled
  * roundup(T, 128) * roundup(C, 4), with C = H / 32 (MXFP8) or H / 16 (NVFP4). */

@@ -18,6 +18,7 @@ from .build import LIB_PATH, build  # noqa: F401  (re-exported)
 
 QUANT = {None: 0, "none": 0, "mxfp8": 1, "nvfp4": 2}
 LAYOUT = {"linear": 0, "swizzled": 1, "128x4": 1}
+EXPERT_LAYOUT = {"grouped": 0, "slot_major": 1}
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1
 MOE_ERR_UNSUPPORTED = 2
@@ -26,7 +27,7 @@ MOE_ERR_INVALID_EXPERT = 4
 MOE_ERR_CUDA = 5
 MOE_ERR_ROW_OUT_OF_RANGE = 6
 MOE_ERR_DEVICE_TIMEOUT = 7
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 
 class MoeCombineArgs(C.Structure):
@@ -38,7 +39,7 @@ class MoeCombineArgs(C.Structure):
         ("shared_out", C.c_void_p), ("residual", C.c_void_p), ("gamma", C.c_void_p),
         ("eps", C.c_float), ("weight_bias", C.c_float),
         ("quant", C.c_int32), ("sf_layout", C.c_int32), ("global_scale", C.c_float),
-        ("reserved0", C.c_int32),
+        ("expert_layout", C.c_int32),
         ("combined_out", C.c_void_p), ("residual_out", C.c_void_p), ("norm_out", C.c_void_p),
         ("quant_out", C.c_void_p), ("scales_out", C.c_void_p), ("status", C.c_void_p),
     ]
@@ -70,6 +71,8 @@ SYMBOLS = {
     "moe_scales_bytes": (C.c_int, [C.c_int64, C.c_int32, C.c_int32, C.c_int32,
                                    C.POINTER(C.c_size_t)]),
     "moe_tuning_set": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
+    "moe_dispatch_permute": (C.c_int, [C.c_void_p, C.c_int64, C.c_int32, C.c_void_p, C.c_int32,
+                                       C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p]),
 }
 
 
@@ -166,6 +169,14 @@ def moe_scales_bytes(T: int, H: int, quant: str, sf_layout: str = "linear") -> i
     return n.value
 
 
+def moe_dispatch_permute(x, row_map, x_grouped, status=None, stream=None) -> None:
+    """x [T, H] bf16 -> x_grouped [n_rows, H]: row row_map[t, j] >= 0 gets x[t]."""
+    T, H = x.shape
+    _check(lib().moe_dispatch_permute(_ptr(x), T, H, _ptr(row_map), row_map.shape[1], _ptr(x_grouped),
+                                      int(x_grouped.shape[0]), _ptr(status), _stream(stream)),
+           "moe_dispatch_permute")
+
+
 def moe_tuning_set(vpt: int = 0, rows_per_slot: int = 0, ring_kib: int = 0, ctas_per_sm: int = 0,
                    route_cluster: int = 0) -> None:
     """Overrides the launch plans (0 = automatic); results do not depend on it."""
@@ -175,16 +186,21 @@ def moe_tuning_set(vpt: int = 0, rows_per_slot: int = 0, ring_kib: int = 0, ctas
 def combine_args(*, expert_out, row_map, router_weights, shared_out=None, residual=None,
                  gamma=None, eps=1e-6, weight_bias=0.0, quant=None, sf_layout="linear",
                  global_scale=1.0, combined_out=None, residual_out=None, norm_out=None,
-                 quant_out=None, scales_out=None, status=None, H=None) -> MoeCombineArgs:
-    """Fills a MoeCombineArgs from tensors (T and top_k from row_map's shape)."""
-    T, k = row_map.shape
+                 quant_out=None, scales_out=None, status=None, H=None,
+                 expert_layout="grouped") -> MoeCombineArgs:
+    """Fills a MoeCombineArgs from tensors (T and top_k from router_weights'
+    shape).  expert_layout "slot_major": expert_out is [top_k, T, H] and
+    row_map may be None."""
+    T, k = router_weights.shape
     if H is None:
-        H = int(expert_out.shape[1])
+        H = int(expert_out.shape[-1])
+    n_rows = int(expert_out.numel() // H) if H else 0
     return MoeCombineArgs(
-        T=T, H=H, top_k=k, expert_out=_ptr(expert_out), n_expert_rows=int(expert_out.shape[0]),
+        T=T, H=H, top_k=k, expert_out=_ptr(expert_out), n_expert_rows=n_rows,
+        expert_layout=EXPERT_LAYOUT[expert_layout],
         row_map=_ptr(row_map), router_weights=_ptr(router_weights), shared_out=_ptr(shared_out),
         residual=_ptr(residual), gamma=_ptr(gamma), eps=eps, weight_bias=weight_bias,
-        quant=QUANT[quant], sf_layout=LAYOUT[sf_layout], global_scale=global_scale, reserved0=0,
+        quant=QUANT[quant], sf_layout=LAYOUT[sf_layout], global_scale=global_scale,
         combined_out=_ptr(combined_out), residual_out=_ptr(residual_out), norm_out=_ptr(norm_out),
         quant_out=_ptr(quant_out), scales_out=_ptr(scales_out), status=_ptr(status))
 

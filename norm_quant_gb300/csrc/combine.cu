@@ -84,6 +84,7 @@ struct Params {
     uint8_t *quant_out, *scales_out;
     int32_t *status;
     int32_t stages, rows;  // ring slots, rows per slot
+    int32_t slot_major;    // expert_out is [k, T, H]: row of (t, j) is j * T + t
     int64_t sf_cols, sf_cols_pad, sf_rows_pad;
 };
 
@@ -180,8 +181,11 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
         int64_t t = blockIdx.x;
         int32_t r_next = -1;
         float w_next = 0.f;
+        auto row_of = [&](int64_t tt) {
+            return p.slot_major ? static_cast<int32_t>(lane * p.T + tt) : __ldg(p.row_map + tt * k + lane);
+        };
         if (t < p.T && lane < k) {
-            r_next = __ldg(p.row_map + t * k + lane);
+            r_next = row_of(t);
             w_next = __ldg(p.weights + t * k + lane);
         }
         for (; t < p.T && ok; t += gridDim.x) {
@@ -189,7 +193,7 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
             const float w = w_next;
             const int64_t tn = t + gridDim.x;
             if (tn < p.T && lane < k) {
-                r_next = __ldg(p.row_map + tn * k + lane);
+                r_next = row_of(tn);
                 w_next = __ldg(p.weights + tn * k + lane);
             }
             bool valid = lane < k && r >= 0;
@@ -614,7 +618,7 @@ extern "C" moe_status moe_combine(const moe_combine_args *a, moe_stream_t stream
 {
     if (!a)
         return MOE_ERR_INVALID_ARG;
-    if (a->T < 0 || a->reserved0 != 0)
+    if (a->T < 0 || (a->expert_layout != MOE_LAYOUT_GROUPED && a->expert_layout != MOE_LAYOUT_SLOT_MAJOR))
         return MOE_ERR_INVALID_ARG;
     if (a->H < 8 || a->H % 8 != 0 || a->top_k < 1)
         return MOE_ERR_INVALID_ARG;
@@ -622,7 +626,10 @@ extern "C" moe_status moe_combine(const moe_combine_args *a, moe_stream_t stream
         return MOE_ERR_UNSUPPORTED;
     if (a->T == 0)
         return MOE_OK;  // an empty batch: empty tensors may carry NULL pointers
-    if (!a->row_map || !a->router_weights || a->n_expert_rows < 0)
+    const bool slot_major = a->expert_layout == MOE_LAYOUT_SLOT_MAJOR;
+    if ((!slot_major && !a->row_map) || !a->router_weights || a->n_expert_rows < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (slot_major && (a->n_expert_rows != a->T * a->top_k || a->T * a->top_k >= (int64_t(1) << 31)))
         return MOE_ERR_INVALID_ARG;
     if (a->n_expert_rows > 0 && !a->expert_out)
         return MOE_ERR_INVALID_ARG;
@@ -660,7 +667,8 @@ extern "C" moe_status moe_combine(const moe_combine_args *a, moe_stream_t stream
     p.k = a->top_k;
     p.expert_out = static_cast<const uint8_t *>(a->expert_out);
     p.n_rows = a->n_expert_rows;
-    p.row_map = a->row_map;
+    p.row_map = slot_major ? nullptr : a->row_map;
+    p.slot_major = slot_major ? 1 : 0;
     p.weights = a->router_weights;
     p.shared = static_cast<const uint8_t *>(a->shared_out);
     p.residual = static_cast<const uint8_t *>(a->residual);

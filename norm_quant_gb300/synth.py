@@ -143,3 +143,21 @@ def make_inputs(wl: Workload, seed: Optional[int] = None) -> dict:
     d["gamma"] = (bf16_normal(rng, (wl.H,), std=wl.gamma_std, mean=wl.gamma_mean)
                   if wl.gamma_mean is not None else None)
     return d
+
+
+def make_slot_major_inputs(wl: Workload, seed: Optional[int] = None) -> dict:
+    """Inputs for the slot-major layout: every token has one expert row per
+    slot, stored as bf16 [k, T, H] (no routing ids, no padding); weights are
+    the softmax of N(0, 1) logits per token as in make_inputs."""
+    rng = np.random.Generator(np.random.PCG64((wl.seed if seed is None else seed) + 500))
+    logits = rng.standard_normal((wl.T, wl.k))
+    w = np.exp(logits - logits.max(axis=1, keepdims=True))
+    w = (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+    d = dict(weights=w, n_valid=wl.T * wl.k)
+    d["expert_out"] = bf16_normal(rng, (wl.k, wl.T, wl.H))
+    d["shared"] = (bf16_normal(rng, (wl.T, wl.H), std=wl.shared_std)
+                   if wl.shared_std is not None else None)
+    d["residual"] = bf16_normal(rng, (wl.T, wl.H)) if wl.residual else None
+    d["gamma"] = (bf16_normal(rng, (wl.H,), std=wl.gamma_std, mean=wl.gamma_mean)
+                  if wl.gamma_mean is not None else None)
+    return d

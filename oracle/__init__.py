@@ -57,6 +57,7 @@ class CombineArgs(C.Structure):
         ("combined_out", C.c_void_p), ("residual_out", C.c_void_p),
         ("norm_out", C.c_void_p), ("quant_out", C.c_void_p),
         ("scales_out", C.c_void_p), ("y_out", C.c_void_p),
+        ("expert_layout", C.c_int32), ("pad0", C.c_int32),
     ]
 
 
@@ -91,6 +92,9 @@ def lib() -> C.CDLL:
             L.oracle_combine_args_size.restype = C.c_int
             L.oracle_combine.restype = C.c_int
             L.oracle_combine.argtypes = [C.POINTER(CombineArgs)]
+            L.oracle_dispatch_permute.restype = C.c_int
+            L.oracle_dispatch_permute.argtypes = [C.c_void_p, C.c_int64, C.c_int32, C.c_void_p,
+                                                  C.c_int32, C.c_void_p, C.c_int64]
             L.oracle_dequant_mxfp8.restype = None
             L.oracle_dequant_mxfp8.argtypes = [C.c_void_p, C.c_void_p, C.c_int64, C.c_int32,
                                                C.c_int32, C.c_void_p]
@@ -190,18 +194,23 @@ def build_row_map(topk_ids: np.ndarray, E: int):
 
 def combine(expert_out, row_map, weights, *, shared=None, residual=None, gamma=None,
             eps=1e-6, weight_bias=0.0, quant=None, sf_layout="linear",
-            global_scale=1.0, outputs=("combined", "residual", "norm", "quant", "y")):
+            global_scale=1.0, outputs=("combined", "residual", "norm", "quant", "y"),
+            expert_layout="grouped"):
     """Run the oracle on host arrays.
 
-    expert_out: uint16 bf16 bits [n_rows, H]; row_map int32 [T, k]; weights
-    fp32 [T, k]; shared / residual: uint16 [T, H] or None; gamma: uint16 [H]
+    expert_out: uint16 bf16 bits [n_rows, H] grouped by expert (row_map int32
+    [T, k]) or, with expert_layout="slot_major", [k, T, H] (row_map unused);
+    weights fp32 [T, k]; shared / residual: uint16 [T, H] or None; gamma: uint16 [H]
     or None (no RMSNorm).  Returns a dict with the requested outputs
     (combined / residual / norm as uint16 bf16 bits, quant + scales as uint8,
     y as the fp64 quantiser input) and 'status'."""
     ex = _c(expert_out, np.uint16)
-    rm = _c(row_map, np.int32)
     w = _c(weights, np.float32)
-    T, k = rm.shape
+    T, k = w.shape
+    slot_major = expert_layout == "slot_major"
+    rm = None if slot_major else _c(row_map, np.int32)
+    if slot_major:
+        ex = ex.reshape(k * T, -1)      # [k, T, H] -> rows j * T + t
     H = ex.shape[1] if ex.ndim == 2 else int(np.asarray(residual if residual is not None
                                                          else shared).shape[1])
     sh = _c(shared, np.uint16)
@@ -227,9 +236,21 @@ def combine(expert_out, row_map, weights, *, shared=None, residual=None, gamma=N
         sf_layout=LAYOUT[sf_layout], global_scale=global_scale,
         combined_out=_ptr(out.get("combined")), residual_out=_ptr(out.get("residual")),
         norm_out=_ptr(out.get("norm")), quant_out=_ptr(out.get("quant")),
-        scales_out=_ptr(out.get("scales")), y_out=_ptr(out.get("y")))
+        scales_out=_ptr(out.get("scales")), y_out=_ptr(out.get("y")),
+        expert_layout=1 if slot_major else 0)
     out["status"] = lib().oracle_combine(C.byref(a))
     return out
+
+
+def dispatch_permute(x: np.ndarray, row_map: np.ndarray, n_rows: int, fill: int = 0):
+    """x_grouped [n_rows, H] (uint16 bf16 bits) with x[t] copied to every row
+    row_map[t, j] >= 0; other rows hold `fill`.  Returns (status, x_grouped)."""
+    xx = _c(x, np.uint16)
+    rm = _c(row_map, np.int32)
+    T, H = xx.shape
+    out = np.full((n_rows, H), fill, np.uint16)
+    st = lib().oracle_dispatch_permute(_ptr(xx), T, H, _ptr(rm), rm.shape[1], _ptr(out), n_rows)
+    return st, out
 
 
 def dequant(q: np.ndarray, scales: np.ndarray, T: int, H: int, quant: str,

@@ -47,7 +47,12 @@
  *  R9 NVFP4 block scale s = e4m3(amax(g*y) / 6); each element is scaled by
  *     the block scale's fp32 reciprocal, q = e2m1(fp32(g*y) * fp32(1/s)),
  *     q = 0 when s == 0; element 2i in the low nibble;
- *  R10 the 128x4 swizzled scale layout of the cuBLAS block-scaling format.
+ *  R10 the 128x4 swizzled scale layout of the cuBLAS block-scaling format;
+ *  R15 the slot-major layout (trtllm_moe_allreduce_fusion,
+ *     moe_reduction_active_experts_token_input / moe_reduction_scale_input /
+ *     moe_reduction_token_input): expert rows as [k, T, H], one per slot, the
+ *     per-(token, slot) scale in the router-weight layout [T, k], and the
+ *     token input added like the shared-expert row.
  */
 #include <math.h>
 #include <stdint.h>
@@ -298,6 +303,10 @@ typedef struct {
     uint8_t *quant_out;         /* [T, H] (MXFP8) or [T, H/2] (NVFP4) or NULL */
     uint8_t *scales_out;        /* oracle_scales_bytes(...) bytes or NULL */
     double *y_out;              /* fp64 [T, H] quantiser input, or NULL */
+    int32_t expert_layout;      /* 0: rows grouped by expert, found through row_map;
+                                   1: slot-major [k, T, H], row of (t, j) at j * T + t,
+                                      row_map unused (reading R15) */
+    int32_t pad0;
 } oracle_combine_args;
 
 int oracle_combine_args_size(void) { return (int)sizeof(oracle_combine_args); }
@@ -378,7 +387,9 @@ int oracle_combine(const oracle_combine_args *a)
         for (int32_t h = 0; h < H; h++)
             s[h] = 0.0;
         for (int32_t j = 0; j < k; j++) {
-            int32_t r = a->row_map[t * k + j];
+            /* slot-major: every slot of every token has its row
+             * (trtllm_moe_allreduce_fusion, moe_reduction_active_experts_token_input) */
+            int64_t r = a->expert_layout == 1 ? (int64_t)j * a->T + t : a->row_map[t * k + j];
             if (r < 0)
                 continue; /* padded slot: contributes nothing */
             if (r >= a->n_rows) {
@@ -435,6 +446,34 @@ int oracle_combine(const oracle_combine_args *a)
     free(s);
     free(x);
     free(y32);
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dispatch-side permute                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* The step before the expert computation, the inverse of the combine's
+ * gather (flashinfer.comm.moe_a2a_combine: combine is the inverse of
+ * moe_a2a_dispatch): token t's row x[t] is copied to every expert-grouped
+ * row row_map[t, j] >= 0.  Rows of x_grouped that no slot names are left as
+ * they are.  Returns ORACLE_ERR_INVALID_ARG if a row_map entry is >= n_rows
+ * (that slot is skipped). */
+int oracle_dispatch_permute(const uint16_t *x, int64_t T, int32_t H, const int32_t *row_map, int32_t k,
+                            uint16_t *x_grouped, int64_t n_rows)
+{
+    int status = ORACLE_OK;
+    for (int64_t t = 0; t < T; t++)
+        for (int32_t j = 0; j < k; j++) {
+            int32_t r = row_map[t * k + j];
+            if (r < 0)
+                continue;
+            if (r >= n_rows) {
+                status = ORACLE_ERR_INVALID_ARG;
+                continue;
+            }
+            memcpy(x_grouped + (int64_t)r * H, x + t * H, sizeof(uint16_t) * (size_t)H);
+        }
     return status;
 }
 

@@ -51,12 +51,13 @@ def gpu_route(ids: np.ndarray, E: int, stream=None):
 
 
 def gpu_combine(wl, inp, d_row_map, *, global_scale=1.0, outputs=None, stream=None,
-                canary=False):
+                canary=False, expert_layout="grouped"):
     """Runs moe_combine for workload `wl` on device copies of `inp`.
     Returns host numpy outputs (bf16 as uint16 bits) and the status word."""
     T, H, k = wl.T, wl.H, wl.k
     outputs = outputs or wl.outputs
     ex = d(inp["expert_out"]) if inp["n_valid"] else torch.zeros((0, H), dtype=torch.int16, device=DEV)
+    ex = ex.reshape(-1, H)
     w = d(inp["weights"])
     sh = d(inp["shared"]) if inp["shared"] is not None else None
     rs = d(inp["residual"]) if inp["residual"] is not None else None
@@ -83,7 +84,7 @@ def gpu_combine(wl, inp, d_row_map, *, global_scale=1.0, outputs=None, stream=No
                     quant=wl.quant, sf_layout=wl.sf_layout, global_scale=global_scale,
                     combined_out=views.get("combined"), residual_out=views.get("residual"),
                     norm_out=views.get("norm"), quant_out=views.get("quant"),
-                    scales_out=views.get("scales"), status=status, H=H)
+                    scales_out=views.get("scales"), status=status, H=H, expert_layout=expert_layout)
     torch.cuda.synchronize()
     res = {"status": int(status.item())}
     for name, v in views.items():
@@ -100,12 +101,18 @@ def gpu_combine(wl, inp, d_row_map, *, global_scale=1.0, outputs=None, stream=No
     return res
 
 
-def oracle_combine(wl, inp, row_map: np.ndarray, *, tokens=None, global_scale=1.0,
-                   sf_layout=None):
+def oracle_combine(wl, inp, row_map, *, tokens=None, global_scale=1.0,
+                   sf_layout=None, expert_layout="grouped"):
     """Oracle outputs for all tokens, or for the listed token rows only
     (then in linear scale layout, indexed by position in `tokens`)."""
     sel = slice(None) if tokens is None else np.asarray(tokens)
     pick = (lambda a: a) if tokens is None else (lambda a: None if a is None else a[sel])
+    if expert_layout == "slot_major":
+        assert tokens is None, "the slot-major oracle runs on whole batches"
+        return oracle.combine(
+            inp["expert_out"], None, inp["weights"], shared=inp["shared"], residual=inp["residual"],
+            gamma=inp["gamma"], eps=wl.eps, weight_bias=wl.weight_bias, quant=wl.quant,
+            sf_layout=sf_layout or wl.sf_layout, global_scale=global_scale, expert_layout="slot_major")
     return oracle.combine(
         inp["expert_out"], row_map[sel], inp["weights"][sel], shared=pick(inp["shared"]),
         residual=pick(inp["residual"]), gamma=inp["gamma"], eps=wl.eps,
@@ -120,13 +127,18 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return 2.0 ** (e - 7)
 
 
-def sum_magnitude(inp, row_map: np.ndarray, tokens) -> np.ndarray:
-    """Per element sum of |terms| of x = sum_j w x_j + shared + residual."""
+def sum_magnitude(inp, row_map, tokens) -> np.ndarray:
+    """Per element sum of |terms| of x = sum_j w x_j + shared + residual
+    (row_map None: the slot-major layout [k, T, H])."""
     tokens = np.asarray(tokens)
-    H = inp["expert_out"].shape[1] if inp["n_valid"] else (
+    H = inp["expert_out"].shape[-1] if inp["n_valid"] else (
         inp["residual"].shape[1] if inp["residual"] is not None else 1)
     mag = np.zeros((tokens.size, H))
     rows = inp["expert_out"]
+    if row_map is None:
+        k, T = rows.shape[0], rows.shape[1]
+        row_map = (np.arange(k)[None, :] * T + np.arange(T)[:, None]).astype(np.int32)
+        rows = rows.reshape(k * T, H)
     for i, t in enumerate(tokens):
         for j in range(row_map.shape[1]):
             r = row_map[t, j]
@@ -186,10 +198,10 @@ def assert_quant_close(wl, got_q, got_s, want_q, want_s, T, H, global_scale, wha
     assert same >= 0.999, f"{what}: only {same:.5f} of code bytes identical"
 
 
-def nvfp4_global_scale(wl, inp, row_map) -> float:
+def nvfp4_global_scale(wl, inp, row_map, expert_layout="grouped") -> float:
     """g = fp32(448 * 6 / amax(y)) over the whole tensor, from the oracle's y."""
     o = oracle.combine(inp["expert_out"], row_map, inp["weights"], shared=inp["shared"],
                        residual=inp["residual"], gamma=inp["gamma"], eps=wl.eps,
-                       weight_bias=wl.weight_bias, outputs=("y",))
+                       weight_bias=wl.weight_bias, outputs=("y",), expert_layout=expert_layout)
     amax = float(np.abs(o["y"]).max())
     return float(np.float32(448.0 * 6.0 / amax)) if amax > 0 else 1.0

@@ -62,7 +62,7 @@ def test_workspace_size_grows_with_slots(L):
 def _args(**kw):
     base = dict(T=4, H=64, top_k=2, expert_out=0x1000, n_expert_rows=8, row_map=0x2000,
                 router_weights=0x3000, shared_out=None, residual=None, gamma=None, eps=1e-6,
-                weight_bias=0.0, quant=0, sf_layout=0, global_scale=1.0, reserved0=0,
+                weight_bias=0.0, quant=0, sf_layout=0, global_scale=1.0, expert_layout=0,
                 combined_out=0x4000, residual_out=None, norm_out=None, quant_out=None,
                 scales_out=None, status=None)
     base.update(kw)
@@ -79,7 +79,8 @@ def _args(**kw):
     (dict(quant=1, quant_out=0x5000, scales_out=0x6000, sf_layout=2), 1),
     (dict(norm_out=0x7000), 1), (dict(expert_out=0x1008), 1), (dict(combined_out=0x4004), 1),
     (dict(row_map=0x2002), 1), (dict(eps=-1.0), 1), (dict(eps=float("nan")), 1),
-    (dict(reserved0=1), 1), (dict(status=0x8002), 1),
+    (dict(expert_layout=2), 1), (dict(status=0x8002), 1),
+    (dict(expert_layout=1, row_map=None, n_expert_rows=7), 1),  # slot-major needs top_k * T rows
     (dict(T=0), 0),  # a valid no-op: returns before any CUDA call
     (dict(T=0, row_map=None, router_weights=None, expert_out=None, combined_out=None), 0),
 ])
@@ -117,3 +118,13 @@ def test_route_validation(L):
     assert L.moe_build_row_map(0x400, 4, 2, 8, 0x100, 0x200, 0x300, None, ws, 8, None) == 3
     assert L.moe_build_row_map(0x400, 4, 2, 8, 0x100, 0x200, 0x300, None, None, 0, None) == 3
     assert L.moe_build_row_map(0x400, 4, 2, 8, None, 0x200, 0x300, None, ws, 1 << 20, None) == 1
+
+
+def test_dispatch_validation(L):
+    assert L.moe_dispatch_permute(0x1000, 4, 60, 0x2000, 2, 0x3000, 8, None, None) == 1   # H % 8
+    assert L.moe_dispatch_permute(0x1000, 4, 32768, 0x2000, 2, 0x3000, 8, None, None) == 2
+    assert L.moe_dispatch_permute(0x1000, 4, 64, 0x2000, 0, 0x3000, 8, None, None) == 1   # top_k
+    assert L.moe_dispatch_permute(None, 4, 64, 0x2000, 2, 0x3000, 8, None, None) == 1
+    assert L.moe_dispatch_permute(0x1008, 4, 64, 0x2000, 2, 0x3000, 8, None, None) == 1   # alignment
+    assert L.moe_dispatch_permute(0x1000, 4, 64, 0x2002, 2, 0x3000, 8, None, None) == 1
+    assert L.moe_dispatch_permute(None, 0, 64, None, 2, None, 0, None, None) == 0          # empty batch

@@ -42,10 +42,11 @@ def route_and_check(ids, E, stream=None):
     return row_map, orm
 
 
-def compare(wl, inp, orm, got, tokens=None, global_scale=1.0):
+def compare(wl, inp, orm, got, tokens=None, global_scale=1.0, expert_layout="grouped"):
     T, H, k = wl.T, wl.H, wl.k
     tok = np.arange(T) if tokens is None else np.asarray(tokens)
-    o = oracle_combine(wl, inp, orm, tokens=None if tokens is None else tok, global_scale=global_scale)
+    o = oracle_combine(wl, inp, orm, tokens=None if tokens is None else tok, global_scale=global_scale,
+                       expert_layout=expert_layout)
     assert o["status"] == 0
     mag = sum_magnitude(inp, orm, tok)
     floor = GAMMA_K(k) * mag
@@ -224,3 +225,57 @@ def test_every_launch_plan_matches_the_oracle(plan):
             run_workload(wl, canary=True)
     finally:
         nqg.moe_tuning_set()
+
+
+@pytest.mark.parametrize("kw", [
+    dict(T=300, H=7168, k=8, shared_std=0.5, quant="mxfp8", outputs=("residual", "quant")),
+    dict(T=257, H=4096, k=8, gamma_mean=0.0, weight_bias=1.0, quant="nvfp4", sf_layout="swizzled",
+         outputs=("residual", "quant")),
+    dict(T=33, H=7200, k=4, shared_std=0.5, outputs=("combined", "residual", "norm")),
+    dict(T=5, H=64, k=1, residual=False, gamma_mean=None, outputs=("combined",)),
+], ids=["prefill_like_mxfp8", "gemma_like_nvfp4", "ragged_h", "k1_gather"])
+def test_slot_major_layout_parity(kw):
+    """The slot-major expert layout [k, T, H] with per-(token, slot) scales
+    (trtllm_moe_allreduce_fusion's moe_reduction_* inputs) against the oracle."""
+    wl = _wl(**{"E": 1, **kw})
+    inp = synth.make_slot_major_inputs(wl)
+    g = nvfp4_global_scale(wl, inp, None, "slot_major") if wl.quant == "nvfp4" else 1.0
+    got = gpu_combine(wl, inp, None, global_scale=g, canary=True, expert_layout="slot_major")
+    assert got["status"] == 0
+    compare(wl, inp, None, got, global_scale=g, expert_layout="slot_major")
+
+
+@pytest.mark.parametrize("T,H,k,E", [(4096, 7168, 8, 256), (1, 8, 1, 1), (333, 7200, 4, 16),
+                                     (2000, 4096, 8, 128), (64, 16384, 8, 256)])
+def test_dispatch_permute_parity(T, H, k, E):
+    """Every expert-grouped row gets its token's row, bit for bit; rows no
+    slot names keep their previous contents."""
+    rng = np.random.Generator(np.random.PCG64(T + H))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    ids[rng.random((T, k)) < 0.1] = -1
+    d_rm, orm = route_and_check(ids, E)
+    nv = int((ids >= 0).sum())
+    x = synth.bf16_normal(rng, (T, H))
+    n_rows = nv + 5
+    xg = torch.full((n_rows, H), 0x3F80, dtype=torch.int16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nqg.moe_dispatch_permute(d(x), d_rm, xg, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    st, want = oracle.dispatch_permute(x, orm, n_rows, fill=0x3F80)
+    assert st == 0
+    assert np.array_equal(h(xg, np.uint16), want)
+
+
+def test_dispatch_permute_reports_out_of_range_rows():
+    T, H, k = 8, 64, 2
+    x = synth.bf16_normal(np.random.Generator(np.random.PCG64(3)), (T, H))
+    rm = np.arange(T * k, dtype=np.int32).reshape(T, k)
+    rm[3, 1] = 10_000
+    xg = torch.zeros((T * k, H), dtype=torch.int16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nqg.moe_dispatch_permute(d(x), d(rm), xg, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == nqg.MOE_ERR_ROW_OUT_OF_RANGE
+    st, want = oracle.dispatch_permute(x, rm, T * k)
+    assert np.array_equal(h(xg, np.uint16), want)

@@ -305,3 +305,38 @@ def test_empty_batch():
     o = oracle.combine(np.zeros((0, 32), np.uint16), np.zeros((0, 2), np.int32),
                        np.zeros((0, 2), np.float32), quant="mxfp8")
     assert o["status"] == 0 and o["quant"].shape == (0, 32)
+
+
+# ------------------------------------------------------- slot-major layout --
+
+def test_slot_major_is_the_grouped_layout_with_row_map_j_T_plus_t():
+    # the slot-major buffer [k, T, H] is a grouped buffer whose row_map is
+    # row_map[t, j] = j * T + t; both index paths must agree bit for bit
+    T, k, H = 37, 4, 64
+    rows = bf(RNG.standard_normal((k, T, H)))
+    w = np.array(RNG.dirichlet(np.ones(k), T), np.float32)
+    kw = dict(shared=bf(RNG.standard_normal((T, H))), residual=bf(RNG.standard_normal((T, H))),
+              gamma=bf(1 + 0.1 * RNG.standard_normal(H)), quant="mxfp8")
+    a = oracle.combine(rows, None, w, expert_layout="slot_major", **kw)
+    rm = (np.arange(k)[None, :] * T + np.arange(T)[:, None]).astype(np.int32)
+    b = oracle.combine(rows.reshape(k * T, H), rm, w, **kw)
+    for key in ("combined", "residual", "norm", "y", "quant", "scales"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_slot_major_one_hot_recovers_slot_and_token():
+    # slot j of token t is the unit vector e_(j*T + t) in H = k*T columns
+    T, k = 6, 3
+    H = k * T + 6
+    rows = np.zeros((k, T, H), np.float32)
+    for j in range(k):
+        for t in range(T):
+            rows[j, t, j * T + t] = 1.0
+    w = np.array([[2.0 ** -(j + 1) for j in range(k)] for _ in range(T)], np.float32)
+    w[2, 1] = 0.0
+    o = oracle.combine(bf(rows), None, w, expert_layout="slot_major", outputs=("combined",))
+    want = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            want[t, j * T + t] = w[t, j]
+    assert np.array_equal(f(o["combined"]), want)
