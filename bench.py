@@ -54,8 +54,11 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--workload", choices=["tiny", "decode", "prefill", "gemma", "padded"],
-                    default="prefill", help="the headline is prefill; the others are for analysis")
+    ap.add_argument("--workload", choices=["tiny", "decode", "prefill", "gemma", "padded",
+                                           "slot_major", "dispatch"],
+                    default="prefill", help="the headline is prefill; the others are for analysis "
+                    "(slot_major: the prefill shape with [k, T, H] expert rows; dispatch: the "
+                    "prefill shape's dispatch-side permute)")
     ap.add_argument("--l2", choices=["none", "write"], default="none",
                     help="none: inputs larger than L2; write: 256 MB write before each step")
     return ap.parse_args()
@@ -87,7 +90,8 @@ def dist_env():
 def workload(name="prefill"):
     from norm_quant_gb300 import synth
     return {"tiny": synth.TINY, "decode": synth.DECODE, "prefill": synth.PREFILL,
-            "gemma": synth.GEMMA_NVFP4, "padded": synth.PADDED}[name]
+            "gemma": synth.GEMMA_NVFP4, "padded": synth.PADDED, "slot_major": synth.PREFILL,
+            "dispatch": synth.PREFILL}[name]
 
 
 def algorithmic_bytes(wl, n_valid: int) -> dict:
@@ -204,7 +208,7 @@ def run_reference(args):
         return
     import oracle
     from norm_quant_gb300 import synth
-    wl = workload(args.workload)
+    wl = workload("prefill")  # the reference arm always times the headline workload
     inp = synth.make_inputs(wl)
     st, _, _, orm, _ = oracle.build_row_map(inp["topk_ids"], wl.E)
     rate, _, _ = cpu_oracle_rate(wl, inp, orm, 1.0)
@@ -261,16 +265,19 @@ def run_ours(args):
     build()
     nqg.lib()
 
-    wl = workload(args.workload)
+    kind = args.workload
+    wl = workload(kind)
     T, H, E, k = wl.T, wl.H, wl.E, wl.k
-    inp = synth.make_inputs(wl)
+    inp = synth.make_slot_major_inputs(wl) if kind == "slot_major" else synth.make_inputs(wl)
+    if kind == "dispatch":  # the residual stream is the token input of the permute
+        inp = {"topk_ids": inp["topk_ids"], "x": inp["residual"], "n_valid": inp["n_valid"]}
 
     def pinned(a):
         a = a.view(np.int16) if a.dtype == np.uint16 else a
         return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
 
-    names = [n for n in ("topk_ids", "weights", "expert_out", "shared", "residual", "gamma")
-             if inp[n] is not None]
+    names = [n for n in ("topk_ids", "weights", "expert_out", "shared", "residual", "gamma", "x")
+             if inp.get(n) is not None]
     host = {n: pinned(inp[n]) for n in names}
     dv = {n: t.to(dev) for n, t in host.items()}
     counts = torch.empty(E, dtype=torch.int32, device=dev)
@@ -278,31 +285,40 @@ def run_ours(args):
     row_map = torch.empty((T, k), dtype=torch.int32, device=dev)
     ws = torch.empty(nqg.moe_build_row_map_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
     outs = {}
+    if kind == "dispatch":
+        outs["x_grouped"] = torch.empty((inp["n_valid"], H), dtype=torch.int16, device=dev)
     for o in ("combined", "residual", "norm"):
-        if o in wl.outputs:
+        if kind != "dispatch" and o in wl.outputs:
             outs[o] = torch.empty((T, H), dtype=torch.int16, device=dev)
-    if wl.quant:
+    if kind != "dispatch" and wl.quant:
         outs["quant"] = torch.empty((T, H if wl.quant == "mxfp8" else H // 2), dtype=torch.uint8, device=dev)
         outs["scales"] = torch.empty(nqg.moe_scales_bytes(T, H, wl.quant, wl.sf_layout), dtype=torch.uint8,
                                      device=dev)
     flush = torch.empty(L2_FLUSH_BYTES if args.l2 == "write" else 16, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    sptr = stream.cuda_stream
-    # NVFP4's per-tensor scale only changes which codes come out, not the work
-    args_c = nqg.combine_args(expert_out=dv["expert_out"], row_map=row_map, router_weights=dv["weights"],
-                              shared_out=dv.get("shared"), residual=dv.get("residual"), gamma=dv.get("gamma"),
-                              eps=wl.eps, weight_bias=wl.weight_bias, quant=wl.quant, sf_layout=wl.sf_layout,
-                              global_scale=1.0, combined_out=outs.get("combined"),
-                              residual_out=outs.get("residual"), norm_out=outs.get("norm"),
-                              quant_out=outs.get("quant"), scales_out=outs.get("scales"), H=H)
-
-    route_kernels = 1 if (T * k <= 524288 and E <= 1024) else 3
+    args_c = None
+    if kind != "dispatch":
+        # NVFP4's per-tensor scale only changes which codes come out, not the work
+        args_c = nqg.combine_args(expert_out=dv["expert_out"].reshape(-1, H),
+                                  row_map=None if kind == "slot_major" else row_map,
+                                  router_weights=dv["weights"], shared_out=dv.get("shared"),
+                                  residual=dv.get("residual"), gamma=dv.get("gamma"), eps=wl.eps,
+                                  weight_bias=wl.weight_bias, quant=wl.quant, sf_layout=wl.sf_layout,
+                                  global_scale=1.0, combined_out=outs.get("combined"),
+                                  residual_out=outs.get("residual"), norm_out=outs.get("norm"),
+                                  quant_out=outs.get("quant"), scales_out=outs.get("scales"), H=H,
+                                  expert_layout="slot_major" if kind == "slot_major" else "grouped")
+    route_kernels = 0 if kind == "slot_major" else (1 if (T * k <= 524288 and E <= 1024) else 3)
 
     def route(st):
-        nqg.moe_build_row_map(dv["topk_ids"], E, counts, offsets, row_map, None, ws, stream=st)
+        if kind != "slot_major":
+            nqg.moe_build_row_map(dv["topk_ids"], E, counts, offsets, row_map, None, ws, stream=st)
 
-    def combine(st):
-        nqg.moe_combine(stream=st, args=args_c)
+    def combine(st):  # the dominant kernel of the step
+        if kind == "dispatch":
+            nqg.moe_dispatch_permute(dv["x"], row_map, outs["x_grouped"], stream=st)
+        else:
+            nqg.moe_combine(stream=st, args=args_c)
 
     def step(st):
         route(st)
@@ -315,7 +331,8 @@ def run_ours(args):
                 flush.zero_()
             step(gs.cuda_stream)
     torch.cuda.synchronize()
-    assert nqg.moe_build_row_map_check(ws, stream=gs.cuda_stream) == nqg.MOE_OK
+    if kind != "slot_major":
+        assert nqg.moe_build_row_map_check(ws, stream=gs.cuda_stream) == nqg.MOE_OK
 
     def graph_of(fn):
         g = torch.cuda.CUDAGraph()
@@ -383,7 +400,11 @@ def run_ours(args):
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
 
     if rank == 0:
-        byt = algorithmic_bytes(wl, inp["n_valid"])
+        if kind == "dispatch":
+            nv = inp["n_valid"]
+            byt = {"total": T * 2 * H + nv * 2 * H + 4 * k * T}
+        else:
+            byt = algorithmic_bytes(wl, inp["n_valid"])
         comb_avg_s = comb_s
         achieved = byt["total"] / comb_avg_s / 1e9
         peak, peak_kind = measured_peak()
@@ -393,8 +414,10 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": wl.name, "T": T, "H": H, "E": E, "top_k": k,
-                       "io": f"bf16 in, fp32 accumulate, out: {'+'.join(wl.outputs)}"
-                             + (f" ({wl.quant}, {wl.sf_layout} scales)" if wl.quant else ""),
+                       "io": ("bf16 token rows copied to expert-grouped rows" if kind == "dispatch" else
+                              f"bf16 in, fp32 accumulate, out: {'+'.join(wl.outputs)}"
+                              + (f" ({wl.quant}, {wl.sf_layout} scales)" if wl.quant else "")
+                              + (", slot-major [k, T, H] expert rows" if kind == "slot_major" else "")),
                        "l2": ("256 MB L2 write-flush before each step, outside the timed events"
                               if args.l2 == "write" else
                               f"no flush: each step streams {byt['total'] / 1e6:.0f} MB through the 129 MB L2"),
@@ -404,14 +427,16 @@ def run_ours(args):
             "achieved_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
-                         "kernel": "combine_kernel", "kernel_ms": comb_avg_s * 1e3,
-                         "algorithmic_bytes": byt["total"], "traffic": recorded_traffic()},
+                         "kernel": "dispatch_kernel" if kind == "dispatch" else "combine_kernel",
+                         "kernel_ms": comb_avg_s * 1e3,
+                         "algorithmic_bytes": byt["total"],
+                         "traffic": recorded_traffic() if kind == "prefill" else None},
             "e2e": {"value": job_throughput(world, T, args.e2e_steps, e2e_s), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": (route_kernels + 1) * K,
             "clocks": clk.summary(),
         }
-        if not args.no_cpu_baseline and world == 1 and wl.residual and wl.shared_std is not None:
+        if not args.no_cpu_baseline and world == 1 and kind == "prefill":
             import oracle
             st, _, _, orm, _ = oracle.build_row_map(inp["topk_ids"], E)
             rate, n, dt = cpu_oracle_rate(wl, inp, orm, args.cpu_seconds)
