@@ -171,6 +171,9 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
         fence_mbar_init();
     }
     __syncthreads();
+    // launched as a programmatic dependent: nothing before this line touches
+    // global memory, so the setup above overlaps the previous kernel's tail
+    grid_dependency_wait();
 
     if (warp == ncw) {
         // ------------------------------------------------------- producer
@@ -576,8 +579,23 @@ moe_status launch_t(const Params &p, const Plan &pl, cudaStream_t stream)
     if (ctas <= 0)
         return MOE_ERR_CUDA;
     const int grid = static_cast<int>(p.T < ctas ? p.T : ctas);
-    kern<<<grid, (pl.ncw + 1) * 32, pl.smem.total, stream>>>(p);
-    return launch_status();
+    // programmatic dependent launch: the kernel may be scheduled while the
+    // previous kernel on the stream finishes; it waits for it before reading
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3((pl.ncw + 1) * 32);
+    cfg.dynamicSmemBytes = pl.smem.total;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
 }
 
 template <int QUANT>

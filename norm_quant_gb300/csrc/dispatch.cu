@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(32) dispatch_kernel(const uint8_t *__restrict_
         fence_mbar_init();
     }
     __syncwarp();
+    grid_dependency_wait();  // see the combine kernel: programmatic dependent launch
 
     auto load = [&](int64_t i) {  // lane 0 only
         const uint32_t s = static_cast<uint32_t>(i % S);
@@ -154,7 +155,20 @@ extern "C" moe_status moe_dispatch_permute(const void *x, int64_t T, int32_t H, 
     if (ctas <= 0)
         return MOE_ERR_CUDA;
     const int grid = static_cast<int>(T < ctas ? T : ctas);
-    dispatch_kernel<<<grid, 32, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint8_t *>(x), T, H, row_map, top_k, static_cast<uint8_t *>(x_grouped), n_rows, status, S);
-    return launch_status();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, dispatch_kernel, static_cast<const uint8_t *>(x), T, H, row_map, top_k,
+                           static_cast<uint8_t *>(x_grouped), n_rows, status, S) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
 }

@@ -20,6 +20,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// ---------------------------------------------------- programmatic launch
+
+// Blocks until the grids this one depends on (programmatic dependent launch)
+// have completed and their memory operations are visible; a no-op when the
+// kernel was launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the grid that depends on this one begin launching (its threads still
+// wait in grid_dependency_wait until this grid has completed).
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)

@@ -17,15 +17,20 @@
 //
 // For N <= kFusedMaxSlots and E <= kFusedMaxExperts the three steps run as
 // ONE launch (route_fused_kernel): a thread-block cluster of up to 16 CTAs
-// (8 where 16 cannot be placed) of 32 warps, one chunk per warp.  Each CTA keeps its chunk histograms in
-// shared memory; after a cluster barrier every CTA reads the per-expert
-// totals of the others through distributed shared memory, derives offsets
-// and its own chunk bases, and scatters.  Cluster barriers are hardware
-// barriers over co-scheduled CTAs, so nothing spins.
+// (8 where 16 cannot be placed) of 32 warps, one chunk per warp.  Each warp
+// counts its chunk into its own column of an expert-major shared histogram;
+// each slot's rank inside its chunk comes from warp ballots over the bits of
+// the expert ids (no atomics); one warp per 8 experts turns the columns into
+// prefixes with shuffle scans; after a cluster barrier every CTA reads the
+// other CTAs' per-expert totals through distributed shared memory, a second
+// barrier ends all remote access, and each CTA derives counts, offsets and
+// its bases locally and scatters.  Cluster barriers are
+// hardware barriers over co-scheduled CTAs, so nothing spins.
 #include <cstdint>
 #include <cuda_runtime.h>
 
 #include "common.h"
+#include "ptx.cuh"
 
 namespace nqg {
 namespace {
@@ -195,6 +200,7 @@ __global__ void route_scatter_kernel(const int32_t *__restrict__ ids, int64_t N,
                                      int32_t *__restrict__ row_map, int32_t *__restrict__ src_row)
 {
     extern __shared__ int32_t sh[];
+    allow_dependent_launch();  // the combine may start its setup now
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t c = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + warp;
     if (c >= chunks)
@@ -240,11 +246,11 @@ int g_route_cluster = 0;  // see set_route_cluster
 constexpr int kFusedThreads = 1024;
 constexpr int kFusedWarps = kFusedThreads / 32;
 constexpr int kFusedMaxCtas = 16;                // non-portable cluster size where allowed
-constexpr int kFusedMaxPerLane = 32;             // chunk <= 1024 slots per warp
+constexpr int kFusedMaxPerLane = 16;             // chunk <= 512 slots per warp
 constexpr int64_t kFusedMaxSlots = int64_t(kFusedMaxCtas) * kFusedWarps * 32 * kFusedMaxPerLane;
-constexpr int kFusedMaxExperts = 1024;
-constexpr int kParts = 4;                        // the cross-warp prefix runs 4-way parallel
-constexpr int kTile = kFusedThreads / kParts;    // experts per prefix pass
+constexpr int kFusedMaxExperts = 512;
+constexpr int kHistPitch = kFusedWarps + 1;      // hist[e][w] at e * 33 + w: banks (e + w) % 32
+constexpr int kScanIlp = 8;                      // experts scanned together by one warp
 
 struct FusedPlan {
     int ctas, per_lane;  // cluster size; slots per lane (chunk = 32 * per_lane per warp)
@@ -253,9 +259,8 @@ struct FusedPlan {
 
 size_t fused_smem(int32_t E)
 {
-    // hist[32][E] + tot[E] + cnt[E] + pre[E] + off[E + 1] + psum[4][256] + wsum[32]
-    return (static_cast<size_t>(kFusedWarps) * E + 4 * static_cast<size_t>(E) + 1 + kParts * kTile + 32) *
-           sizeof(int32_t);
+    // hist[E][33] + all_tot[16][E] + base[E] + off[E + 1] + wsum[32]
+    return (static_cast<size_t>(kHistPitch + kFusedMaxCtas + 2) * E + 1 + 32) * sizeof(int32_t);
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -282,7 +287,8 @@ __device__ __forceinline__ int32_t ld_dsmem(const int32_t *local, uint32_t rank)
 
 // One cluster of gridDim.x CTAs (the whole grid), 32 warps each; warp w of
 // CTA b owns the chunk of PL * 32 consecutive slots starting at
-// (b * 32 + w) * PL * 32.  Every thread reaches every barrier.
+// (b * 32 + w) * PL * 32, taken 32 at a time in order.  Every thread
+// reaches every barrier.
 template <int PL>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     route_fused_kernel(const int32_t *__restrict__ ids, int64_t N, int32_t E, int32_t *__restrict__ counts,
@@ -290,110 +296,123 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                        int32_t *__restrict__ src_row, int32_t *__restrict__ err)
 {
     extern __shared__ int32_t sh[];
-    int32_t *hist = sh;                                          // [32][E]
-    int32_t *tot = hist + static_cast<size_t>(kFusedWarps) * E;  // [E] this CTA's totals (read remotely)
-    int32_t *cnt = tot + E;                                      // [E] cluster-wide counts
-    int32_t *pre = cnt + E;                                      // [E] counts of lower-ranked CTAs
-    int32_t *off = pre + E;                                      // [E + 1] offsets
-    int32_t *psum = off + E + 1;                                 // [4][256] part sums
-    int32_t *wsum = psum + kParts * kTile;                       // [32] scan scratch
+    int32_t *hist = sh;                                               // [E][33]: warp counts, then prefixes
+    int32_t *all_tot = hist + static_cast<size_t>(kHistPitch) * E;    // [16][E]
+    int32_t *base = all_tot + static_cast<size_t>(kFusedMaxCtas) * E;  // [E]: offsets + lower CTAs
+    int32_t *off = base + E;                                          // [E + 1]
+    int32_t *wsum = off + E + 1;                                      // [32]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const int nctas = static_cast<int>(gridDim.x);
     const int64_t first = (static_cast<int64_t>(rank) * kFusedWarps + warp) * (PL * 32);
-    const int part = threadIdx.x / kTile, el = threadIdx.x % kTile;
+    const uint32_t lt = (1u << lane) - 1u;
+    allow_dependent_launch();  // the combine may start its setup now
 
-    // 1. chunk histograms
-    int32_t *h = hist + static_cast<size_t>(warp) * E;
+    // 1. each warp counts its chunk into its own column of hist and ranks
+    //    every slot among the earlier slots of the chunk with the same expert.
+    //    Per 32 slots, a lane's peers (lanes holding the same expert) come
+    //    from one ballot per bit of the expert id; its rank is the running
+    //    count plus the peers below it, and the lowest peer alone advances
+    //    the count (the column is this warp's, so no atomics are needed)
     for (int e = lane; e < E; e += 32)
-        h[e] = 0;
-    int32_t v[PL];
+        hist[e * kHistPitch + warp] = 0;
+    int32_t v[PL], rk[PL];
 #pragma unroll
     for (int it = 0; it < PL; ++it) {
         const int64_t i = first + it * 32 + lane;
         v[it] = (i < N) ? __ldg(ids + i) : -1;
     }
+    const int key_bits = 32 - __clz(E);  // ids 0..E-1 and the key E of an invalid slot
     __syncwarp();
     bool bad = false;
 #pragma unroll
     for (int it = 0; it < PL; ++it) {
         const int32_t e = v[it];
-        if (e >= 0 && e < E)
-            atomicAdd(&h[e], 1);
-        else if (e != -1)
-            bad = true;
+        const bool valid = e >= 0 && e < E;
+        bad |= !valid && e != -1;
+        const uint32_t key = valid ? static_cast<uint32_t>(e) : static_cast<uint32_t>(E);
+        uint32_t peers = 0xffffffffu;
+        for (int b = 0; b < key_bits; ++b) {
+            const bool bit = (key >> b) & 1u;
+            const uint32_t on = __ballot_sync(0xffffffffu, bit);
+            peers &= bit ? on : ~on;
+        }
+        rk[it] = valid ? hist[e * kHistPitch + warp] + __popc(peers & lt) : 0;
+        __syncwarp();
+        if (valid && (peers & lt) == 0)  // the lowest lane of the group
+            hist[e * kHistPitch + warp] += __popc(peers);
+        __syncwarp();
     }
-    // the error word is cleared by CTA 0 before the first cluster barrier and
-    // only OR-ed into after it
+    // the error word is cleared by CTA 0 before the cluster barrier and only
+    // OR-ed into after it
     if (rank == 0 && threadIdx.x == 0)
         *err = 0;
     __syncthreads();
-    // 2. exclusive prefix over this CTA's 32 warps per expert: part p of the
-    //    threads owns warps [8p, 8p + 8), then the parts combine in smem
-    for (int e0 = 0; e0 < E; e0 += kTile) {
-        const int e = e0 + el;
-        int32_t run = 0;
-        if (e < E) {
+    // 2. per expert: exclusive prefix over the 32 warp columns (a shuffle
+    //    scan, kScanIlp experts at a time per warp) and the CTA's total
+    for (int e0 = warp * kScanIlp; e0 < E; e0 += kFusedWarps * kScanIlp) {
+        int32_t x[kScanIlp], incl[kScanIlp];
 #pragma unroll
-            for (int i = 0; i < kFusedWarps / kParts; ++i) {
-                int32_t *cell = &hist[static_cast<size_t>(part * (kFusedWarps / kParts) + i) * E + e];
-                const int32_t x = *cell;
-                *cell = run;
-                run += x;
-            }
-            psum[part * kTile + el] = run;
+        for (int q = 0; q < kScanIlp; ++q) {
+            x[q] = (e0 + q < E) ? hist[(e0 + q) * kHistPitch + lane] : 0;
+            incl[q] = x[q];
         }
-        __syncthreads();
-        if (e < E) {
-            int32_t before = 0, all = 0;
 #pragma unroll
-            for (int q = 0; q < kParts; ++q) {
-                const int32_t x = psum[q * kTile + el];
-                before += (q < part) ? x : 0;
-                all += x;
+        for (int d = 1; d < 32; d <<= 1)
+#pragma unroll
+            for (int q = 0; q < kScanIlp; ++q) {
+                const int32_t o = __shfl_up_sync(0xffffffffu, incl[q], d);
+                if (lane >= d)
+                    incl[q] += o;
             }
-            if (before)
 #pragma unroll
-                for (int i = 0; i < kFusedWarps / kParts; ++i)
-                    hist[static_cast<size_t>(part * (kFusedWarps / kParts) + i) * E + e] += before;
-            if (part == 0)
-                tot[e] = all;
+        for (int q = 0; q < kScanIlp; ++q) {
+            const int e = e0 + q;
+            if (e < E) {
+                hist[e * kHistPitch + lane] = incl[q] - x[q];
+                if (lane == 31)
+                    all_tot[rank * E + e] = incl[q];  // this CTA's total, in its own row
+            }
         }
-        __syncthreads();
     }
-    // 3. publish totals to the cluster; each CTA reads every CTA's totals
+    // 3. publish the totals; every CTA pulls the other CTAs' rows (all loads
+    //    in flight at once); the second barrier keeps every CTA alive until
+    //    no one reads its shared memory any more
     cluster_sync_all();
     if (__any_sync(0xffffffffu, bad) && lane == 0)
         atomicOr(err, 1);
     for (int e = threadIdx.x; e < E; e += kFusedThreads) {
         int32_t x[kFusedMaxCtas];
 #pragma unroll
-        for (int b = 0; b < kFusedMaxCtas; ++b)  // all remote reads in flight at once
-            x[b] = (b < nctas) ? ld_dsmem(tot + e, static_cast<uint32_t>(b)) : 0;
-        int32_t all = 0, before = 0;
+        for (int b = 0; b < kFusedMaxCtas; ++b)
+            x[b] = (b < nctas && b != static_cast<int>(rank)) ? ld_dsmem(&all_tot[b * E + e], static_cast<uint32_t>(b)) : 0;
 #pragma unroll
-        for (int b = 0; b < kFusedMaxCtas; ++b) {
-            all += x[b];
-            before += (b < static_cast<int>(rank)) ? x[b] : 0;
-        }
-        cnt[e] = all;
-        pre[e] = before;
+        for (int b = 0; b < kFusedMaxCtas; ++b)
+            if (b < nctas && b != static_cast<int>(rank))
+                all_tot[b * E + e] = x[b];
     }
-    // 4. no CTA reads another's shared memory after this barrier, so any CTA
-    //    may run ahead and exit
     cluster_sync_all();
-    // 5. exclusive scan of cnt over experts (one contiguous range per thread)
+    // 4. counts, exclusive scan over experts, this CTA's base per expert
     {
-        const int per_t = (E + kFusedThreads - 1) / kFusedThreads;
+        const int per_t = (E + kFusedThreads - 1) / kFusedThreads;  // 1 for E <= 1024
         const int ea = threadIdx.x * per_t, eb = (ea + per_t < E) ? ea + per_t : E;
         int32_t s = 0;
-        for (int e = ea; e < eb; ++e)
-            s += cnt[e];
+        for (int e = ea; e < eb; ++e) {
+            int32_t all = 0, before = 0;
+            for (int b = 0; b < nctas; ++b) {
+                const int32_t x = all_tot[b * E + e];
+                all += x;
+                before += (b < static_cast<int>(rank)) ? x : 0;
+            }
+            off[e] = all;      // the count, for now
+            base[e] = before;  // lower CTAs' share, for now
+            s += all;
+        }
         int32_t incl = s;
 #pragma unroll
-        for (int dd = 1; dd < 32; dd <<= 1) {
-            const int32_t o = __shfl_up_sync(0xffffffffu, incl, dd);
-            if (lane >= dd)
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d)
                 incl += o;
         }
         if (lane == 31)
@@ -403,9 +422,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             const int32_t ws = wsum[lane];
             int32_t wi = ws;
 #pragma unroll
-            for (int dd = 1; dd < 32; dd <<= 1) {
-                const int32_t o = __shfl_up_sync(0xffffffffu, wi, dd);
-                if (lane >= dd)
+            for (int d = 1; d < 32; d <<= 1) {
+                const int32_t o = __shfl_up_sync(0xffffffffu, wi, d);
+                if (lane >= d)
                     wi += o;
             }
             wsum[lane] = wi - ws;  // exclusive prefix of warp sums
@@ -415,51 +434,32 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         __syncthreads();
         int32_t run = wsum[warp] + incl - s;
         for (int e = ea; e < eb; ++e) {
+            const int32_t c = off[e];
+            if (rank == 0) {
+                counts[e] = c;
+                offsets[e] = run;
+            }
             off[e] = run;
-            run += cnt[e];
+            base[e] += run;
+            run += c;
         }
-    }
-    __syncthreads();
-    if (rank == 0) {
-        for (int e = threadIdx.x; e < E; e += kFusedThreads) {
-            counts[e] = cnt[e];
-            offsets[e] = off[e];
-        }
-        if (threadIdx.x == 0)
+        if (rank == 0 && threadIdx.x == 0)
             offsets[E] = off[E];
     }
-    // 6. chunk bases: offsets + lower CTAs + lower warps of this CTA
-    for (int e0 = 0; e0 < E; e0 += kTile) {
-        const int e = e0 + el;
-        if (e < E) {
-            const int32_t base = off[e] + pre[e];
-#pragma unroll
-            for (int i = 0; i < kFusedWarps / kParts; ++i)
-                hist[static_cast<size_t>(part * (kFusedWarps / kParts) + i) * E + e] += base;
-        }
-    }
     __syncthreads();
-    // 7. stable scatter of this warp's chunk
-    const uint32_t lt = (1u << lane) - 1u;
+    // 5. scatter: row = offsets + lower CTAs + lower warps + rank in the chunk
 #pragma unroll
     for (int it = 0; it < PL; ++it) {
         const int64_t i = first + it * 32 + lane;
         const int32_t e = v[it];
-        const bool valid = (e >= 0) && (e < E);
-        const uint32_t peers = __match_any_sync(0xffffffffu, valid ? e : -1);
-        const int r = __popc(peers & lt);
-        if (valid) {
-            const int32_t row = h[e] + r;
+        if (e >= 0 && e < E) {
+            const int32_t row = base[e] + hist[e * kHistPitch + warp] + rk[it];
             row_map[i] = row;
             if (src_row)
                 src_row[row] = static_cast<int32_t>(i);
         } else if (i < N) {
             row_map[i] = -1;
         }
-        __syncwarp();
-        if (valid && r == 0)
-            h[e] += __popc(peers);
-        __syncwarp();
     }
 }
 
@@ -472,8 +472,7 @@ FusedFn fused_fn(int per_lane)
     case 2: return route_fused_kernel<2>;
     case 4: return route_fused_kernel<4>;
     case 8: return route_fused_kernel<8>;
-    case 16: return route_fused_kernel<16>;
-    default: return route_fused_kernel<32>;
+    default: return route_fused_kernel<16>;
     }
 }
 
@@ -486,7 +485,7 @@ bool fused_fits(FusedFn fn, int per_lane, int ctas, size_t smem)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return false;
-    const int pl_idx = per_lane == 1 ? 0 : per_lane == 2 ? 1 : per_lane == 4 ? 2 : per_lane == 8 ? 3 : per_lane == 16 ? 4 : 5;
+    const int pl_idx = per_lane == 1 ? 0 : per_lane == 2 ? 1 : per_lane == 4 ? 2 : per_lane == 8 ? 3 : 4;
     const int bucket = static_cast<int>((smem + 32 * 1024 - 1) / (32 * 1024));
     if (bucket >= 8 || static_cast<size_t>(bucket) * 32 * 1024 > 227 * 1024)
         return false;
