@@ -56,7 +56,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 /* Limits of this implementation (validated on the host). */
 #define MOE_MAX_TOP_K 32
@@ -80,9 +80,29 @@ typedef enum {
 typedef enum {
     MOE_QUANT_NONE = 0,
     MOE_QUANT_MXFP8 = 1, /* e4m3 codes [T, H] bytes + UE8M0 scale per 32 elements */
-    MOE_QUANT_NVFP4 = 2  /* e2m1 codes [T, H/2] bytes (element 2i in the low nibble)
+    MOE_QUANT_NVFP4 = 2, /* e2m1 codes [T, H/2] bytes (element 2i in the low nibble)
                             + e4m3 scale per 16 elements, with global scale g */
+    MOE_QUANT_MXFP4 = 3  /* e2m1 codes [T, H/2] bytes (element 2i in the low nibble)
+                            + UE8M0 scale per 32 elements: the smallest e with
+                            amax <= 6 * 2^e, biased by 127 (global_scale ignored) */
 } moe_quant_kind;
+
+/* Element type of every 16-bit tensor of a combine call: expert_out,
+ * shared_out, residual, gamma and the combined / residual / norm outputs
+ * (Struct_ep_combine_skip_a2a -- combine_dtype; trtllm_moe_allreduce_fusion --
+ * "fp16/bf16 -> fp4"). */
+typedef enum {
+    MOE_IO_BF16 = 0,
+    MOE_IO_FP16 = 1
+} moe_io_dtype;
+
+/* Element type of router_weights (Struct_ep_combine_skip_a2a --
+ * router_weights_dtype); weights are widened to fp32 exactly. */
+typedef enum {
+    MOE_WEIGHTS_FP32 = 0,
+    MOE_WEIGHTS_BF16 = 1,
+    MOE_WEIGHTS_FP16 = 2
+} moe_weight_dtype;
 
 typedef enum {
     MOE_LAYOUT_GROUPED = 0,    /* expert_out rows grouped by expert; row_map[t, j] gives
@@ -192,31 +212,33 @@ typedef struct moe_combine_args {
     int64_t T;                    /* tokens (rows of every [T, *] tensor); 0 = no-op */
     int32_t H;                    /* hidden size; multiple of 8, <= MOE_MAX_HIDDEN */
     int32_t top_k;                /* slots per token, 1..MOE_MAX_TOP_K */
-    const void *expert_out;       /* device bf16 [n_expert_rows, H]: grouped by expert,
+    const void *expert_out;       /* device [n_expert_rows, H] (io_dtype): grouped by expert,
                                      or [top_k, T, H] slot-major (see expert_layout) */
     int64_t n_expert_rows;        /* rows in expert_out (row_map entries must be below;
                                      exactly top_k * T for the slot-major layout) */
     const int32_t *row_map;       /* device int32 [T, top_k], -1 = padded slot; unused
                                      (may be NULL) for the slot-major layout */
-    const float *router_weights;  /* device fp32 [T, top_k], used as given */
-    const void *shared_out;       /* device bf16 [T, H] or NULL: shared-expert row, weight 1 */
-    const void *residual;         /* device bf16 [T, H] or NULL */
-    const void *gamma;            /* device bf16 [H] or NULL = no RMSNorm */
+    const void *router_weights;   /* device [T, top_k] (weight_dtype), used as given */
+    const void *shared_out;       /* device [T, H] (io_dtype) or NULL: shared-expert row, weight 1 */
+    const void *residual;         /* device [T, H] (io_dtype) or NULL */
+    const void *gamma;            /* device [H] (io_dtype) or NULL = no RMSNorm */
     float eps;                    /* RMSNorm epsilon, >= 0, inside the square root */
     float weight_bias;            /* added to gamma: 0 standard, 1 Gemma form */
     int32_t quant;                /* moe_quant_kind */
     int32_t sf_layout;            /* moe_sf_layout (ignored when quant == NONE) */
     float global_scale;           /* NVFP4 g > 0: codes encode g * y (ignored otherwise) */
     int32_t expert_layout;        /* moe_expert_layout */
-    void *combined_out;           /* device bf16 [T, H] or NULL: bf16(s) */
-    void *residual_out;           /* device bf16 [T, H] or NULL: bf16(x) */
-    void *norm_out;               /* device bf16 [T, H] or NULL: bf16(y); needs gamma */
-    void *quant_out;              /* device uint8: [T, H] MXFP8 / [T, H/2] NVFP4; needs quant */
+    void *combined_out;           /* device [T, H] (io_dtype) or NULL: s rounded */
+    void *residual_out;           /* device [T, H] (io_dtype) or NULL: x rounded */
+    void *norm_out;               /* device [T, H] (io_dtype) or NULL: y rounded; needs gamma */
+    void *quant_out;              /* device uint8: [T, H] MXFP8 / [T, H/2] NVFP4, MXFP4; needs quant */
     void *scales_out;             /* device uint8, moe_scales_bytes(...) bytes; needs quant */
     int32_t *status;              /* device int32 or NULL: set to a nonzero moe_status
                                      if the kernel meets a row_map entry >= n_expert_rows
                                      (that slot is skipped) or a bounded wait gives up;
                                      the caller zeroes it beforehand */
+    int32_t io_dtype;             /* moe_io_dtype (0: bf16) */
+    int32_t weight_dtype;         /* moe_weight_dtype (0: fp32) */
 } moe_combine_args;
 
 /* Enqueues the combine on `stream`.
@@ -232,8 +254,10 @@ typedef struct moe_combine_args {
  *   the grouped layout; n_expert_rows == top_k * T < 2^31 for the slot-major one;
  *   expert_out non-NULL when n_expert_rows > 0; every bf16 / byte tensor
  *   pointer 16-byte aligned; at least one output requested;
- *   norm_out needs gamma; quant in {NONE, MXFP8, NVFP4}; MXFP8 needs
- *   H % 32 == 0, NVFP4 needs H % 16 == 0 and a finite global_scale > 0;
+ *   norm_out needs gamma; quant in {NONE, MXFP8, NVFP4, MXFP4}; MXFP8 and
+ *   MXFP4 need H % 32 == 0, NVFP4 needs H % 16 == 0 and a finite
+ *   global_scale > 0; io_dtype and weight_dtype valid (weights 4-byte
+ *   aligned if fp32, 2-byte otherwise);
  *   quant needs quant_out and scales_out; sf_layout in {LINEAR, SWIZZLED}.
  * Returns MOE_OK (enqueued), MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED or
  * MOE_ERR_CUDA. */
@@ -276,7 +300,8 @@ moe_status moe_dispatch_permute(const void *x, int64_t T, int32_t H, const int32
                                 moe_stream_t stream);
 
 /* Bytes of the scale matrix for T rows of H elements: linear T * C, swizzled
- * roundup(T, 128) * roundup(C, 4), with C = H / 32 (MXFP8) or H / 16 (NVFP4). */
+ * roundup(T, 128) * roundup(C, 4), with C = H / 32 (MXFP8, MXFP4) or H / 16
+ * (NVFP4). */
 moe_status moe_scales_bytes(int64_t T, int32_t H, int32_t quant, int32_t sf_layout,
                             size_t *bytes);
 

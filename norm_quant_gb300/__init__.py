@@ -16,7 +16,9 @@ import threading
 
 from .build import LIB_PATH, build  # noqa: F401  (re-exported)
 
-QUANT = {None: 0, "none": 0, "mxfp8": 1, "nvfp4": 2}
+QUANT = {None: 0, "none": 0, "mxfp8": 1, "nvfp4": 2, "mxfp4": 3}
+IO_DTYPE = {"bf16": 0, "fp16": 1}
+WEIGHT_DTYPE = {"fp32": 0, "bf16": 1, "fp16": 2}
 LAYOUT = {"linear": 0, "swizzled": 1, "128x4": 1}
 EXPERT_LAYOUT = {"grouped": 0, "slot_major": 1}
 MOE_OK = 0
@@ -27,7 +29,7 @@ MOE_ERR_INVALID_EXPERT = 4
 MOE_ERR_CUDA = 5
 MOE_ERR_ROW_OUT_OF_RANGE = 6
 MOE_ERR_DEVICE_TIMEOUT = 7
-ABI_VERSION = 2
+ABI_VERSION = 3
 
 
 class MoeCombineArgs(C.Structure):
@@ -42,6 +44,7 @@ class MoeCombineArgs(C.Structure):
         ("expert_layout", C.c_int32),
         ("combined_out", C.c_void_p), ("residual_out", C.c_void_p), ("norm_out", C.c_void_p),
         ("quant_out", C.c_void_p), ("scales_out", C.c_void_p), ("status", C.c_void_p),
+        ("io_dtype", C.c_int32), ("weight_dtype", C.c_int32),
     ]
 
 
@@ -187,7 +190,7 @@ def combine_args(*, expert_out, row_map, router_weights, shared_out=None, residu
                  gamma=None, eps=1e-6, weight_bias=0.0, quant=None, sf_layout="linear",
                  global_scale=1.0, combined_out=None, residual_out=None, norm_out=None,
                  quant_out=None, scales_out=None, status=None, H=None,
-                 expert_layout="grouped") -> MoeCombineArgs:
+                 expert_layout="grouped", io_dtype="bf16", weight_dtype="fp32") -> MoeCombineArgs:
     """Fills a MoeCombineArgs from tensors (T and top_k from router_weights'
     shape).  expert_layout "slot_major": expert_out is [top_k, T, H] and
     row_map may be None."""
@@ -202,7 +205,8 @@ def combine_args(*, expert_out, row_map, router_weights, shared_out=None, residu
         residual=_ptr(residual), gamma=_ptr(gamma), eps=eps, weight_bias=weight_bias,
         quant=QUANT[quant], sf_layout=LAYOUT[sf_layout], global_scale=global_scale,
         combined_out=_ptr(combined_out), residual_out=_ptr(residual_out), norm_out=_ptr(norm_out),
-        quant_out=_ptr(quant_out), scales_out=_ptr(scales_out), status=_ptr(status))
+        quant_out=_ptr(quant_out), scales_out=_ptr(scales_out), status=_ptr(status),
+        io_dtype=IO_DTYPE[io_dtype], weight_dtype=WEIGHT_DTYPE[weight_dtype])
 
 
 def moe_combine(stream=None, **kw) -> None:

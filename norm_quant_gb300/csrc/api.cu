@@ -53,7 +53,7 @@ extern "C" moe_status moe_scales_bytes(int64_t T, int32_t H, int32_t quant, int3
     if (!bytes || T < 0 || H < 1)
         return MOE_ERR_INVALID_ARG;
     int64_t vec;
-    if (quant == MOE_QUANT_MXFP8)
+    if (quant == MOE_QUANT_MXFP8 || quant == MOE_QUANT_MXFP4)
         vec = 32;
     else if (quant == MOE_QUANT_NVFP4)
         vec = 16;

@@ -1,0 +1,675 @@
+// combine_impl.cuh -- the combine kernel template, its launch plan and
+// launchers, shared by combine.cu (bf16 I/O) and combine_f16.cu (fp16 I/O).
+// What the kernel computes and how it is laid out is described in combine.cu.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.h"
+#include "ptx.cuh"
+
+namespace nqg {
+namespace combine_detail {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kMaxStages = 32;
+constexpr size_t kSmemBudget = 200 * 1024;
+constexpr size_t kDefaultRingBytes = 144 * 1024;
+
+// Consumer warps allowed per CTA for each VPT (vectors of 8 elements per
+// consumer thread); the CTA adds one producer warp.  Together they cover
+// H <= 7168 (VPT 1), 8192 (VPT 2, 4) and 16384 (VPT 8).
+template <int VPT>
+__host__ __device__ constexpr int max_consumer_warps() { return VPT == 1 ? 28 : (VPT == 2 ? 16 : 8); }
+inline int max_consumer_warps_rt(int vpt) { return vpt == 1 ? 28 : (vpt == 2 ? 16 : 8); }
+// Rows a ring slot may hold, bounded by the registers the loads take.
+template <int VPT>
+__host__ __device__ constexpr int max_rows() { return VPT <= 2 ? 4 : (VPT == 4 ? 2 : 1); }
+inline int max_rows_rt(int vpt) { return vpt <= 2 ? 4 : (vpt == 4 ? 2 : 1); }
+
+enum : int32_t { F_LAST = 1, F_RESID = 2 };
+
+struct StageMeta {
+    int32_t t;
+    int32_t n;      // rows in the slot, 0..R
+    int32_t flags;  // F_LAST: the token's last slot; F_RESID: its last row is the residual
+    int32_t pad;
+    float w[4];     // weight of each row (1 for the shared and residual rows)
+};
+
+struct Params {
+    int64_t T;
+    int32_t H, k;
+    const uint8_t *expert_out;
+    int64_t n_rows;
+    const int32_t *row_map;
+    const void *weights;
+    const uint8_t *shared;
+    const uint8_t *residual;
+    const uint16_t *gamma;
+    float eps, wb, gscale;
+    int32_t weight_dtype;  // moe_weight_dtype of router_weights
+    int32_t sf_layout;
+    uint16_t *combined_out, *residual_out, *norm_out;
+    uint8_t *quant_out, *scales_out;
+    int32_t *status;
+    int32_t stages, rows;  // ring slots, rows per slot
+    int32_t slot_major;    // expert_out is [k, T, H]: row of (t, j) is j * T + t
+    int64_t sf_cols, sf_cols_pad, sf_rows_pad;
+};
+
+struct SmemLayout {
+    uint32_t row_stride, slot_stride, bars, meta, red, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int32_t H, int32_t stages, int32_t rows, int32_t ncw)
+{
+    SmemLayout L;
+    L.row_stride = (static_cast<uint32_t>(H) * 2u + 127u) & ~127u;
+    L.slot_stride = L.row_stride * static_cast<uint32_t>(rows);
+    L.bars = static_cast<uint32_t>(stages) * L.slot_stride;
+    L.meta = L.bars + (2u * stages + 2u) * 8u;  // full[S], empty[S], reduction barrier, pad
+    L.red = L.meta + static_cast<uint32_t>(stages) * static_cast<uint32_t>(sizeof(StageMeta));
+    L.total = L.red + 2u * static_cast<uint32_t>(ncw) * 4u;
+    return L;
+}
+
+__device__ __forceinline__ void report(int32_t *status, int32_t code)
+{
+    if (status)
+        atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t c, const Params &p)
+{
+    if (p.sf_layout == MOE_SF_LINEAR)
+        return r * p.sf_cols + c;
+    return (r >> 7) * (p.sf_cols_pad >> 2) * 512 + (c >> 2) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (c & 3);
+}
+
+// UE8M0 byte of a block whose absolute maximum is `amax` (>= 0, finite):
+// the smallest e with amax <= 448 * 2^e -- with amax = m * 2^p, m in [1, 2),
+// that is e = p - 8 when m <= 1.75 and p - 7 otherwise -- biased by 127 and
+// clamped to [0, 254].
+__device__ __forceinline__ int32_t ue8m0_byte(float amax)
+{
+    const uint32_t bits = __float_as_uint(amax);
+    const int32_t ef = static_cast<int32_t>(bits >> 23);
+    if (ef == 0)
+        return 0;  // zero or below 2^-126: e <= -134 clamps to 0
+    const int32_t p = ef - 127;
+    const int32_t e = ((bits & 0x7FFFFFu) <= 0x600000u) ? p - 8 : p - 7;
+    const int32_t b = e + 127;
+    return b < 0 ? 0 : (b > 254 ? 254 : b);
+}
+
+// 16-bit element codecs: IO 0 = bf16, 1 = fp16.
+template <int IO>
+__device__ __forceinline__ void unpack16x2(uint32_t w, float &lo, float &hi)
+{
+    if constexpr (IO == 0) {
+        bf16x2_to_f32(w, lo, hi);
+    } else {
+        f16x2_to_f32(w, lo, hi);
+    }
+}
+
+template <int IO>
+__device__ __forceinline__ uint32_t pack16x2(float lo, float hi)
+{
+    if constexpr (IO == 0)
+        return f32x2_to_bf16x2(lo, hi);
+    else
+        return f32x2_to_f16x2(lo, hi);
+}
+
+template <int IO>
+__device__ __forceinline__ void store16x8(uint16_t *base, int64_t off, const float *v)
+{
+    uint4 q;
+    q.x = pack16x2<IO>(v[0], v[1]);
+    q.y = pack16x2<IO>(v[2], v[3]);
+    q.z = pack16x2<IO>(v[4], v[5]);
+    q.w = pack16x2<IO>(v[6], v[7]);
+    *reinterpret_cast<uint4 *>(base + off) = q;
+}
+
+// Router weight idx as fp32: stored as fp32, bf16 or fp16 (moe_weight_dtype).
+__device__ __forceinline__ float load_weight(const void *w, int64_t idx, int32_t dtype)
+{
+    if (dtype == MOE_WEIGHTS_FP32)
+        return __ldg(static_cast<const float *>(w) + idx);
+    const uint32_t b = __ldg(static_cast<const unsigned short *>(w) + idx);
+    if (dtype == MOE_WEIGHTS_BF16)
+        return __uint_as_float(b << 16);
+    float lo, hi;
+    f16x2_to_f32(b, lo, hi);
+    return lo;
+}
+
+// UE8M0 byte for MXFP4: the smallest e with amax <= 6 * 2^e -- with
+// amax = m * 2^p, e = p - 2 when m <= 1.5 and p - 1 otherwise -- biased by
+// 127 and clamped to [0, 254].
+__device__ __forceinline__ int32_t ue8m0_fp4_byte(float amax)
+{
+    const uint32_t bits = __float_as_uint(amax);
+    const int32_t ef = static_cast<int32_t>(bits >> 23);
+    if (ef == 0)
+        return 0;
+    const int32_t p = ef - 127;
+    const int32_t e = ((bits & 0x7FFFFFu) <= 0x400000u) ? p - 2 : p - 1;
+    const int32_t b = e + 127;
+    return b < 0 ? 0 : (b > 254 ? 254 : b);
+}
+
+template <int VPT, int QUANT, int IO>
+__global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combine_kernel(const Params p)
+{
+    constexpr int RMAX = max_rows<VPT>();
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ncw = (blockDim.x >> 5) - 1;
+    const int NC = ncw * 32;
+    const int S = p.stages;
+    const int R = p.rows;
+    const int32_t H = p.H, k = p.k;
+    const int32_t nvec = H >> 3;
+    const uint32_t row_bytes = static_cast<uint32_t>(H) * 2u;
+    const SmemLayout L = smem_layout(H, S, R, ncw);
+    const uint32_t ring = smem_u32(smem);
+    const uint32_t full0 = ring + L.bars, empty0 = full0 + 8u * S, redbar = empty0 + 8u * S;
+    StageMeta *meta = reinterpret_cast<StageMeta *>(smem + L.meta);
+    float *red = reinterpret_cast<float *>(smem + L.red);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, ncw);
+        }
+        mbar_init(redbar, ncw);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // launched as a programmatic dependent: nothing before this line touches
+    // global memory, so the setup above overlaps the previous kernel's tail
+    grid_dependency_wait();
+
+    if (warp == ncw) {
+        // ------------------------------------------------------- producer
+        int stage = 0;
+        uint32_t phase = 0;
+        int64_t issued = 0;
+        bool ok = true;
+        int64_t t = blockIdx.x;
+        int32_t r_next = -1;
+        float w_next = 0.f;
+        auto row_of = [&](int64_t tt) {
+            return p.slot_major ? static_cast<int32_t>(lane * p.T + tt) : __ldg(p.row_map + tt * k + lane);
+        };
+        if (t < p.T && lane < k) {
+            r_next = row_of(t);
+            w_next = load_weight(p.weights, t * k + lane, p.weight_dtype);
+        }
+        for (; t < p.T && ok; t += gridDim.x) {
+            const int32_t r = r_next;
+            const float w = w_next;
+            const int64_t tn = t + gridDim.x;
+            if (tn < p.T && lane < k) {
+                r_next = row_of(tn);
+                w_next = load_weight(p.weights, tn * k + lane, p.weight_dtype);
+            }
+            bool valid = lane < k && r >= 0;
+            if (valid && r >= p.n_rows) {
+                report(p.status, MOE_ERR_ROW_OUT_OF_RANGE);
+                valid = false;
+            }
+            uint32_t mrem = __ballot_sync(0xffffffffu, valid);
+            const int n_exp = __popc(mrem);
+            const bool has_sh = p.shared != nullptr, has_res = p.residual != nullptr;
+            const int n = n_exp + (has_sh ? 1 : 0) + (has_res ? 1 : 0);
+            int i = 0;
+            do {  // one ring slot per iteration; a token with no rows still gets one
+                const int ns = (n - i < R) ? n - i : R;
+                const uint8_t *src[RMAX];
+                float wt[RMAX];
+#pragma unroll
+                for (int q = 0; q < RMAX; ++q) {
+                    src[q] = nullptr;
+                    wt[q] = 1.f;
+                    const int ii = i + q;
+                    if (q < ns) {  // warp-uniform
+                        if (ii < n_exp) {
+                            const int j = __ffs(mrem) - 1;
+                            mrem &= mrem - 1;
+                            const int32_t rj = __shfl_sync(0xffffffffu, r, j);
+                            wt[q] = __shfl_sync(0xffffffffu, w, j);
+                            src[q] = p.expert_out + static_cast<int64_t>(rj) * row_bytes;
+                        } else if (has_sh && ii == n_exp) {
+                            src[q] = p.shared + t * row_bytes;
+                        } else {
+                            src[q] = p.residual + t * row_bytes;
+                        }
+                    }
+                }
+                const bool last = (i + ns >= n);
+                bool good = true;
+                if (lane == 0) {
+                    good = mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, kWaitLimitNs);
+                    if (good) {
+                        StageMeta &m = meta[stage];
+                        m.t = static_cast<int32_t>(t);
+                        m.n = ns;
+                        m.flags = (last ? F_LAST : 0) | ((last && has_res && ns > 0) ? F_RESID : 0);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            m.w[q] = q < RMAX ? wt[q < RMAX ? q : 0] : 1.f;
+                        const uint32_t full = full0 + 8u * stage;
+                        if (ns > 0) {
+                            mbar_arrive_expect_tx(full, static_cast<uint32_t>(ns) * row_bytes);
+                            const uint32_t dst = ring + static_cast<uint32_t>(stage) * L.slot_stride;
+#pragma unroll
+                            for (int q = 0; q < RMAX; ++q)
+                                if (q < ns)
+                                    bulk_g2s(dst + static_cast<uint32_t>(q) * L.row_stride, src[q], row_bytes, full);
+                        } else {
+                            mbar_arrive(full);
+                        }
+                    }
+                }
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (!good) {
+                    ok = false;
+                    break;
+                }
+                ++issued;
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                i += ns;
+            } while (i < n);
+        }
+        if (!ok && lane == 0) {
+            // a slot never freed up: record it, then let every copy this warp
+            // started land before the CTA's shared memory goes away
+            report(p.status, MOE_ERR_DEVICE_TIMEOUT);
+            const int64_t nn = issued < S ? issued : S;
+            for (int64_t s = 0; s < nn; ++s) {
+                const int64_t times = (issued - 1 - s) / S + 1;
+                mbar_wait_bounded(full0 + 8u * static_cast<uint32_t>(s), static_cast<uint32_t>((times - 1) & 1),
+                                  kWaitLimitNs);
+            }
+        }
+        return;
+    }
+
+    // ----------------------------------------------------------- consumers
+    const int tid = threadIdx.x;
+    // pad rows of a swizzled scale matrix are written as zero
+    if (QUANT != MOE_QUANT_NONE && p.sf_layout == MOE_SF_SWIZZLED_128x4 && p.sf_rows_pad > p.T) {
+        const int64_t nz = (p.sf_rows_pad - p.T) * p.sf_cols_pad;
+        for (int64_t i = static_cast<int64_t>(blockIdx.x) * NC + tid; i < nz;
+             i += static_cast<int64_t>(gridDim.x) * NC)
+            p.scales_out[sf_offset(p.T + i / p.sf_cols_pad, i % p.sf_cols_pad, p)] = 0;
+    }
+    const bool do_norm = p.gamma != nullptr;
+    const int max_slots = k + 3;  // a token never needs more slots than rows + 1
+
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t tok = 0;
+    for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, ++tok) {
+        float acc[VPT][8];
+#pragma unroll
+        for (int s = 0; s < VPT; ++s)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                acc[s][i] = 0.f;
+        bool combined_done = false;
+        for (int it = 0; it < max_slots; ++it) {
+            if (!mbar_wait_bounded(full0 + 8u * stage, phase, kWaitLimitNs)) {
+                report(p.status, MOE_ERR_DEVICE_TIMEOUT);
+                return;
+            }
+            const StageMeta m = meta[stage];
+            const uint8_t *slot = smem + static_cast<uint32_t>(stage) * L.slot_stride;
+            uint4 q[RMAX][VPT];
+#pragma unroll
+            for (int rr = 0; rr < RMAX; ++rr)
+#pragma unroll
+                for (int s = 0; s < VPT; ++s) {
+                    const int v = s * NC + tid;
+                    q[rr][s] = make_uint4(0, 0, 0, 0);
+                    if (rr < m.n && v < nvec)
+                        q[rr][s] = *reinterpret_cast<const uint4 *>(slot + rr * L.row_stride + 16 * v);
+                }
+#pragma unroll
+            for (int rr = 0; rr < RMAX; ++rr) {
+                if (rr >= m.n)
+                    break;
+                if ((m.flags & F_RESID) && rr == m.n - 1 && p.combined_out) {
+#pragma unroll
+                    for (int s = 0; s < VPT; ++s) {
+                        const int v = s * NC + tid;
+                        if (v < nvec)
+                            store16x8<IO>(p.combined_out, t * H + 8 * v, acc[s]);
+                    }
+                    combined_done = true;
+                }
+                const float wr = m.w[rr];
+#pragma unroll
+                for (int s = 0; s < VPT; ++s) {
+                    const int v = s * NC + tid;
+                    if (v < nvec) {
+                        const uint32_t qw[4] = {q[rr][s].x, q[rr][s].y, q[rr][s].z, q[rr][s].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            float lo, hi;
+                            unpack16x2<IO>(qw[i], lo, hi);
+                            fma2(acc[s][2 * i], acc[s][2 * i + 1], lo, hi, wr);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(empty0 + 8u * stage);
+            if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            if (m.flags & F_LAST)
+                break;
+        }
+
+        // ------------------------------------------------------ epilogue
+        const int64_t row0 = t * H;
+        if (p.combined_out && !combined_done) {
+#pragma unroll
+            for (int s = 0; s < VPT; ++s) {
+                const int v = s * NC + tid;
+                if (v < nvec)
+                    store16x8<IO>(p.combined_out, row0 + 8 * v, acc[s]);
+            }
+        }
+        if (p.residual_out) {
+#pragma unroll
+            for (int s = 0; s < VPT; ++s) {
+                const int v = s * NC + tid;
+                if (v < nvec)
+                    store16x8<IO>(p.residual_out, row0 + 8 * v, acc[s]);
+            }
+        }
+        if (do_norm) {
+            // gamma is re-read per token; it stays in L1 / L2
+            uint4 gq[VPT];
+#pragma unroll
+            for (int s = 0; s < VPT; ++s) {
+                const int v = s * NC + tid;
+                gq[s] = (v < nvec) ? __ldg(reinterpret_cast<const uint4 *>(p.gamma) + v) : make_uint4(0, 0, 0, 0);
+            }
+            float ss = 0.f;
+#pragma unroll
+            for (int s = 0; s < VPT; ++s)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    ss = fmaf(acc[s][i], acc[s][i], ss);  // vectors past H hold 0
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1)
+                ss += __shfl_xor_sync(0xffffffffu, ss, d);
+            float *part = red + (tok & 1u) * ncw;
+            if (lane == 0) {
+                part[warp] = ss;
+                mbar_arrive(redbar);
+            }
+            if (!mbar_wait_bounded(redbar, tok & 1u, kWaitLimitNs)) {
+                report(p.status, MOE_ERR_DEVICE_TIMEOUT);
+                return;
+            }
+            float total = 0.f;
+            for (int w = 0; w < ncw; ++w)
+                total += part[w];
+            const float rinv = 1.0f / sqrtf(total / static_cast<float>(H) + p.eps);
+#pragma unroll
+            for (int s = 0; s < VPT; ++s) {
+                const uint32_t gv[4] = {gq[s].x, gq[s].y, gq[s].z, gq[s].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float lo, hi;
+                    unpack16x2<IO>(gv[i], lo, hi);
+                    acc[s][2 * i] = acc[s][2 * i] * rinv * (lo + p.wb);
+                    acc[s][2 * i + 1] = acc[s][2 * i + 1] * rinv * (hi + p.wb);
+                }
+            }
+            if (p.norm_out) {
+#pragma unroll
+                for (int s = 0; s < VPT; ++s) {
+                    const int v = s * NC + tid;
+                    if (v < nvec)
+                        store16x8<IO>(p.norm_out, row0 + 8 * v, acc[s]);
+                }
+            }
+        }
+
+        if constexpr (QUANT == MOE_QUANT_MXFP8) {
+#pragma unroll
+            for (int s = 0; s < VPT; ++s) {
+                const int v = s * NC + tid;
+                const bool vv = v < nvec;
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    amax = fmaxf(amax, fabsf(acc[s][i]));
+                amax = vv ? amax : 0.f;
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                const int32_t byte = ue8m0_byte(amax);
+                const float scale = __uint_as_float(static_cast<uint32_t>(254 - byte) << 23);  // 2^-e
+                if (vv) {
+                    uint2 qv;
+                    qv.x = cvt_e4m3x4(acc[s][0] * scale, acc[s][1] * scale, acc[s][2] * scale, acc[s][3] * scale);
+                    qv.y = cvt_e4m3x4(acc[s][4] * scale, acc[s][5] * scale, acc[s][6] * scale, acc[s][7] * scale);
+                    *reinterpret_cast<uint2 *>(p.quant_out + row0 + 8 * v) = qv;
+                    if ((lane & 3) == 0) {
+                        const int64_t c = v >> 2;
+                        p.scales_out[sf_offset(t, c, p)] = static_cast<uint8_t>(byte);
+                        if (c == p.sf_cols - 1)
+                            for (int64_t cp = p.sf_cols; cp < p.sf_cols_pad; ++cp)
+                                p.scales_out[sf_offset(t, cp, p)] = 0;
+                    }
+                }
+            }
+        } else if constexpr (QUANT == MOE_QUANT_MXFP4) {
+#pragma unroll
+            for (int s = 0; s < VPT; ++s) {
+                const int v = s * NC + tid;
+                const bool vv = v < nvec;
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    amax = fmaxf(amax, fabsf(acc[s][i]));
+                amax = vv ? amax : 0.f;
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                const int32_t byte = ue8m0_fp4_byte(amax);
+                const float scale = __uint_as_float(static_cast<uint32_t>(254 - byte) << 23);  // 2^-e
+                if (vv) {
+                    float qv[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        qv[i] = acc[s][i] * scale;
+                    *reinterpret_cast<uint32_t *>(p.quant_out + (row0 >> 1) + 4 * v) = cvt_e2m1x8(qv);
+                    if ((lane & 3) == 0) {
+                        const int64_t c = v >> 2;
+                        p.scales_out[sf_offset(t, c, p)] = static_cast<uint8_t>(byte);
+                        if (c == p.sf_cols - 1)
+                            for (int64_t cp = p.sf_cols; cp < p.sf_cols_pad; ++cp)
+                                p.scales_out[sf_offset(t, cp, p)] = 0;
+                    }
+                }
+            }
+        } else if constexpr (QUANT == MOE_QUANT_NVFP4) {
+#pragma unroll
+            for (int s = 0; s < VPT; ++s) {
+                const int v = s * NC + tid;
+                const bool vv = v < nvec;
+                float g[8];
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    g[i] = acc[s][i] * p.gscale;
+                    amax = fmaxf(amax, fabsf(g[i]));
+                }
+                amax = vv ? amax : 0.f;
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                const uint32_t sc = cvt_e4m3x2(__fdiv_rn(amax, 6.0f), 0.f) & 0xFFu;
+                const float sf = e4m3_code_value(sc);
+                if (vv) {
+                    uint32_t packed = 0;
+                    if (sf != 0.f) {
+                        // elements are scaled by the block scale's correctly
+                        // rounded fp32 reciprocal
+                        const float rs = __frcp_rn(sf);
+                        float qv[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            qv[i] = g[i] * rs;
+                        packed = cvt_e2m1x8(qv);
+                    }
+                    *reinterpret_cast<uint32_t *>(p.quant_out + (row0 >> 1) + 4 * v) = packed;
+                    if ((lane & 1) == 0) {
+                        const int64_t c = v >> 1;
+                        p.scales_out[sf_offset(t, c, p)] = static_cast<uint8_t>(sc);
+                        if (c == p.sf_cols - 1)
+                            for (int64_t cp = p.sf_cols; cp < p.sf_cols_pad; ++cp)
+                                p.scales_out[sf_offset(t, cp, p)] = 0;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------- host
+
+// Process-wide plan overrides set by moe_tuning_set (0 = automatic).
+struct Tuning {
+    int vpt = 0, rows = 0, ring_kib = 0, ctas_per_sm = 0;
+};
+extern Tuning g_tuning;
+
+struct Plan {
+    int vpt, ncw, rows, stages, ctas_per_sm;
+    SmemLayout smem;
+};
+
+// Vectors per consumer thread: the smallest of 1, 2, 4, 8 that needs at most
+// 16 consumer warps.  Rows per ring slot: as many as the registers allow (4
+// for VPT <= 2).  Measured on GB300: at H = 7168, 14 warps x 2 vectors with 4
+// rows per slot reach 93 % of HBM copy bandwidth, against 73 % for 7 warps x 4
+// (latency-bound) and 80 % for 28 warps x 1 (per-row overhead); at H = 4096,
+// 16 warps x 1 beat 8 x 2.  Ring: about kDefaultRingBytes of rows, at least 2
+// slots, within the shared-memory budget.
+inline Plan make_plan(int32_t H)
+{
+    const Tuning tu = g_tuning;
+    Plan pl{};
+    const int nvec = H / 8;
+    auto covers = [&](int v) { return (nvec + 32 * v - 1) / (32 * v) <= max_consumer_warps_rt(v); };
+    pl.vpt = 8;
+    if (tu.vpt && covers(tu.vpt)) {
+        pl.vpt = tu.vpt;
+    } else {
+        for (int v : {1, 2, 4, 8}) {
+            if (covers(v) && (nvec + 32 * v - 1) / (32 * v) <= 16) {
+                pl.vpt = v;
+                break;
+            }
+        }
+    }
+    pl.ncw = (nvec + 32 * pl.vpt - 1) / (32 * pl.vpt);
+    const int rmax = max_rows_rt(pl.vpt);
+    pl.rows = tu.rows ? (tu.rows < rmax ? tu.rows : rmax) : rmax;
+    pl.ctas_per_sm = tu.ctas_per_sm ? tu.ctas_per_sm : 1;
+    // one CTA keeps kSmemBudget; several share the SM's 228 KB (1 KB reserved each)
+    const size_t budget = pl.ctas_per_sm == 1 ? kSmemBudget : (224 * 1024) / pl.ctas_per_sm - 2048;
+    const SmemLayout one = smem_layout(H, 1, pl.rows, pl.ncw);
+    const size_t per_slot = one.slot_stride + 16 + sizeof(StageMeta);
+    const size_t fixed = one.total - per_slot;
+    const size_t ring = tu.ring_kib ? static_cast<size_t>(tu.ring_kib) * 1024 : kDefaultRingBytes;
+    int s = static_cast<int>((ring + one.slot_stride / 2) / one.slot_stride);
+    const int fit = budget > fixed ? static_cast<int>((budget - fixed) / per_slot) : 0;
+    s = s > fit ? fit : s;
+    s = s > kMaxStages ? kMaxStages : s;
+    pl.stages = s < 2 ? 2 : s;
+    pl.smem = smem_layout(H, pl.stages, pl.rows, pl.ncw);
+    return pl;
+}
+
+template <int VPT, int QUANT, int IO>
+moe_status launch_t(const Params &p, const Plan &pl, cudaStream_t stream)
+{
+    auto kern = combine_kernel<VPT, QUANT, IO>;
+    static int configured_for[64] = {0};  // per device: dynamic smem already allowed
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const int need = static_cast<int>(pl.smem.total);
+    if (need > 227 * 1024)
+        return MOE_ERR_UNSUPPORTED;
+    if (dev < 0 || dev >= 64 || configured_for[dev] < need) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, need) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (dev >= 0 && dev < 64)
+            configured_for[dev] = need;
+    }
+    const int64_t ctas = static_cast<int64_t>(sm_count()) * pl.ctas_per_sm;
+    if (ctas <= 0)
+        return MOE_ERR_CUDA;
+    const int grid = static_cast<int>(p.T < ctas ? p.T : ctas);
+    // programmatic dependent launch: the kernel may be scheduled while the
+    // previous kernel on the stream finishes; it waits for it before reading
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3((pl.ncw + 1) * 32);
+    cfg.dynamicSmemBytes = pl.smem.total;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+template <int QUANT, int IO>
+moe_status launch_q(const Params &p, const Plan &pl, cudaStream_t stream)
+{
+    switch (pl.vpt) {
+    case 1: return launch_t<1, QUANT, IO>(p, pl, stream);
+    case 2: return launch_t<2, QUANT, IO>(p, pl, stream);
+    case 4: return launch_t<4, QUANT, IO>(p, pl, stream);
+    default: return launch_t<8, QUANT, IO>(p, pl, stream);
+    }
+}
+
+// Every kernel of one 16-bit I/O type; each type is compiled in its own
+// translation unit (combine.cu: bf16, combine_f16.cu: fp16).
+template <int IO>
+moe_status launch_io(const Params &p, const Plan &pl, int32_t quant, cudaStream_t stream)
+{
+    switch (quant) {
+    case MOE_QUANT_MXFP8: return launch_q<MOE_QUANT_MXFP8, IO>(p, pl, stream);
+    case MOE_QUANT_NVFP4: return launch_q<MOE_QUANT_NVFP4, IO>(p, pl, stream);
+    case MOE_QUANT_MXFP4: return launch_q<MOE_QUANT_MXFP4, IO>(p, pl, stream);
+    default: return launch_q<MOE_QUANT_NONE, IO>(p, pl, stream);
+    }
+}
+
+} // namespace combine_detail
+} // namespace nqg

@@ -172,6 +172,25 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float &lo, float &hi)
     hi = __uint_as_float(w & 0xFFFF0000u);
 }
 
+// fp16x2 (as a 32-bit word) -> two fp32, exact.
+__device__ __forceinline__ void f16x2_to_f32(uint32_t w, float &lo, float &hi)
+{
+    asm("{ .reg .f16 l, h;\n"
+        "  mov.b32 {l, h}, %2;\n"
+        "  cvt.f32.f16 %0, l;\n"
+        "  cvt.f32.f16 %1, h; }"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w));
+}
+
+// Two fp32 -> fp16x2, round to nearest even; `lo` in the low half.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // acc = w * x + acc on two fp32 lanes at once (packed FMA, each lane rounded
 // to nearest exactly like fmaf).
 __device__ __forceinline__ void fma2(float &acc_lo, float &acc_hi, float x_lo, float x_hi, float w)

@@ -50,6 +50,8 @@ class Workload:
     sf_layout: str = "linear"            # "linear" | "swizzled"
     outputs: tuple = ("combined",)       # subset of combined/residual/norm/quant
     seed: int = 0
+    io_dtype: str = "bf16"               # element type of the 16-bit tensors: bf16 | fp16
+    weight_dtype: str = "fp32"           # router weights: fp32 | bf16 | fp16
 
     def with_T(self, T: int, seed: Optional[int] = None) -> "Workload":
         return dataclasses.replace(self, T=T, seed=self.seed if seed is None else seed)
@@ -116,8 +118,14 @@ def draw_routing(wl: Workload, rng: np.random.Generator):
     return ids, w
 
 
-def bf16_normal(rng: np.random.Generator, shape, std=1.0, mean=0.0) -> np.ndarray:
-    """bf16 bit patterns of N(mean, std) draws, generated in row blocks."""
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> IEEE binary16 bit patterns, round to nearest even."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def bf16_normal(rng: np.random.Generator, shape, std=1.0, mean=0.0, io="bf16") -> np.ndarray:
+    """bf16 (or, with io="fp16", binary16) bit patterns of N(mean, std)
+    draws, generated in row blocks."""
     out = np.empty(shape, np.uint16)
     flat = out.reshape(-1, shape[-1]) if len(shape) > 1 else out.reshape(1, -1)
     rows_per = max(1, (1 << 24) // max(1, flat.shape[1]))
@@ -126,8 +134,17 @@ def bf16_normal(rng: np.random.Generator, shape, std=1.0, mean=0.0) -> np.ndarra
         x = rng.standard_normal((r1 - r0, flat.shape[1]), dtype=np.float32)
         if std != 1.0 or mean != 0.0:
             x = x * np.float32(std) + np.float32(mean)
-        flat[r0:r1] = f32_to_bf16_bits(x)
+        flat[r0:r1] = f32_to_f16_bits(x) if io == "fp16" else f32_to_bf16_bits(x)
     return out
+
+
+def weights_as(w: np.ndarray, dtype: str) -> np.ndarray:
+    """fp32 router weights stored as fp32, or as bf16 / fp16 bit patterns."""
+    if dtype == "bf16":
+        return f32_to_bf16_bits(w)
+    if dtype == "fp16":
+        return f32_to_f16_bits(w)
+    return w
 
 
 def make_inputs(wl: Workload, seed: Optional[int] = None) -> dict:
@@ -135,12 +152,13 @@ def make_inputs(wl: Workload, seed: Optional[int] = None) -> dict:
     rng = np.random.Generator(np.random.PCG64(wl.seed if seed is None else seed))
     ids, w = draw_routing(wl, rng)
     n_valid = int((ids >= 0).sum())
-    d = dict(topk_ids=ids, weights=w, n_valid=n_valid)
-    d["expert_out"] = bf16_normal(rng, (n_valid, wl.H))
-    d["shared"] = (bf16_normal(rng, (wl.T, wl.H), std=wl.shared_std)
+    io = wl.io_dtype
+    d = dict(topk_ids=ids, weights=weights_as(w, wl.weight_dtype), n_valid=n_valid)
+    d["expert_out"] = bf16_normal(rng, (n_valid, wl.H), io=io)
+    d["shared"] = (bf16_normal(rng, (wl.T, wl.H), std=wl.shared_std, io=io)
                    if wl.shared_std is not None else None)
-    d["residual"] = bf16_normal(rng, (wl.T, wl.H)) if wl.residual else None
-    d["gamma"] = (bf16_normal(rng, (wl.H,), std=wl.gamma_std, mean=wl.gamma_mean)
+    d["residual"] = bf16_normal(rng, (wl.T, wl.H), io=io) if wl.residual else None
+    d["gamma"] = (bf16_normal(rng, (wl.H,), std=wl.gamma_std, mean=wl.gamma_mean, io=io)
                   if wl.gamma_mean is not None else None)
     return d
 
@@ -153,11 +171,12 @@ def make_slot_major_inputs(wl: Workload, seed: Optional[int] = None) -> dict:
     logits = rng.standard_normal((wl.T, wl.k))
     w = np.exp(logits - logits.max(axis=1, keepdims=True))
     w = (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
-    d = dict(weights=w, n_valid=wl.T * wl.k)
-    d["expert_out"] = bf16_normal(rng, (wl.k, wl.T, wl.H))
-    d["shared"] = (bf16_normal(rng, (wl.T, wl.H), std=wl.shared_std)
+    io = wl.io_dtype
+    d = dict(weights=weights_as(w, wl.weight_dtype), n_valid=wl.T * wl.k)
+    d["expert_out"] = bf16_normal(rng, (wl.k, wl.T, wl.H), io=io)
+    d["shared"] = (bf16_normal(rng, (wl.T, wl.H), std=wl.shared_std, io=io)
                    if wl.shared_std is not None else None)
-    d["residual"] = bf16_normal(rng, (wl.T, wl.H)) if wl.residual else None
-    d["gamma"] = (bf16_normal(rng, (wl.H,), std=wl.gamma_std, mean=wl.gamma_mean)
+    d["residual"] = bf16_normal(rng, (wl.T, wl.H), io=io) if wl.residual else None
+    d["gamma"] = (bf16_normal(rng, (wl.H,), std=wl.gamma_std, mean=wl.gamma_mean, io=io)
                   if wl.gamma_mean is not None else None)
     return d

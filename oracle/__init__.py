@@ -26,7 +26,9 @@ _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-QUANT = {None: 0, "none": 0, "mxfp8": 1, "nvfp4": 2}
+QUANT = {None: 0, "none": 0, "mxfp8": 1, "nvfp4": 2, "mxfp4": 3}
+IO_DTYPE = {"bf16": 0, "fp16": 1}
+WEIGHT_DTYPE = {"fp32": 0, "bf16": 1, "fp16": 2}
 LAYOUT = {"linear": 0, "swizzled": 1, "128x4": 1}
 
 
@@ -57,7 +59,8 @@ class CombineArgs(C.Structure):
         ("combined_out", C.c_void_p), ("residual_out", C.c_void_p),
         ("norm_out", C.c_void_p), ("quant_out", C.c_void_p),
         ("scales_out", C.c_void_p), ("y_out", C.c_void_p),
-        ("expert_layout", C.c_int32), ("pad0", C.c_int32),
+        ("expert_layout", C.c_int32), ("io_dtype", C.c_int32), ("weight_dtype", C.c_int32),
+        ("pad0", C.c_int32),
     ]
 
 
@@ -70,6 +73,15 @@ def lib() -> C.CDLL:
             L.oracle_bf16_to_f64.argtypes = [C.c_uint16]
             L.oracle_f64_to_bf16.restype = C.c_uint16
             L.oracle_f64_to_bf16.argtypes = [C.c_double]
+            L.oracle_f16_to_f64.restype = C.c_double
+            L.oracle_f16_to_f64.argtypes = [C.c_uint16]
+            L.oracle_f64_to_f16.restype = C.c_uint16
+            L.oracle_f64_to_f16.argtypes = [C.c_double]
+            L.oracle_ue8m0_fp4_for_amax.restype = C.c_uint8
+            L.oracle_ue8m0_fp4_for_amax.argtypes = [C.c_double]
+            L.oracle_dequant_mxfp4.restype = None
+            L.oracle_dequant_mxfp4.argtypes = [C.c_void_p, C.c_void_p, C.c_int64, C.c_int32,
+                                               C.c_int32, C.c_void_p]
             L.oracle_e4m3_to_f64.restype = C.c_double
             L.oracle_e4m3_to_f64.argtypes = [C.c_uint8]
             L.oracle_e4m3_from_f64.restype = C.c_uint8
@@ -126,6 +138,29 @@ def f64_to_bf16(x) -> np.ndarray:
     f = lib().oracle_f64_to_bf16
     x = np.asarray(x, dtype=np.float64)
     return np.array([f(float(v)) for v in x.ravel()], dtype=np.uint16).reshape(x.shape)
+
+
+_F16_TABLE = None
+
+
+def f16_to_f64(bits) -> np.ndarray:
+    global _F16_TABLE
+    if _F16_TABLE is None:
+        f = lib().oracle_f16_to_f64
+        _F16_TABLE = np.array([f(i) for i in range(1 << 16)], dtype=np.float64)
+    return _F16_TABLE[np.asarray(bits, dtype=np.uint16)]
+
+
+def f64_to_f16(x) -> np.ndarray:
+    f = lib().oracle_f64_to_f16
+    x = np.asarray(x, dtype=np.float64)
+    return np.array([f(float(v)) for v in x.ravel()], dtype=np.uint16).reshape(x.shape)
+
+
+def ue8m0_fp4_for_amax(amax) -> np.ndarray:
+    f = lib().oracle_ue8m0_fp4_for_amax
+    a = np.asarray(amax, dtype=np.float64)
+    return np.array([f(float(v)) for v in a.ravel()], dtype=np.uint8).reshape(a.shape)
 
 
 def e4m3_to_f64(codes) -> np.ndarray:
@@ -195,17 +230,18 @@ def build_row_map(topk_ids: np.ndarray, E: int):
 def combine(expert_out, row_map, weights, *, shared=None, residual=None, gamma=None,
             eps=1e-6, weight_bias=0.0, quant=None, sf_layout="linear",
             global_scale=1.0, outputs=("combined", "residual", "norm", "quant", "y"),
-            expert_layout="grouped"):
+            expert_layout="grouped", io_dtype="bf16", weight_dtype="fp32"):
     """Run the oracle on host arrays.
 
     expert_out: uint16 bf16 bits [n_rows, H] grouped by expert (row_map int32
     [T, k]) or, with expert_layout="slot_major", [k, T, H] (row_map unused);
     weights fp32 [T, k]; shared / residual: uint16 [T, H] or None; gamma: uint16 [H]
     or None (no RMSNorm).  Returns a dict with the requested outputs
-    (combined / residual / norm as uint16 bf16 bits, quant + scales as uint8,
+    (combined / residual / norm as uint16 bf16 or fp16 bits (io_dtype),
+    quant + scales as uint8,
     y as the fp64 quantiser input) and 'status'."""
     ex = _c(expert_out, np.uint16)
-    w = _c(weights, np.float32)
+    w = _c(weights, np.float32 if weight_dtype == "fp32" else np.uint16)
     T, k = w.shape
     slot_major = expert_layout == "slot_major"
     rm = None if slot_major else _c(row_map, np.int32)
@@ -225,7 +261,7 @@ def combine(expert_out, row_map, weights, *, shared=None, residual=None, gamma=N
         out["norm"] = np.zeros((T, H), np.uint16)
     qk = QUANT[quant]
     if qk and "quant" in outputs:
-        out["quant"] = np.zeros((T, H if qk == 1 else H // 2), np.uint8)
+        out["quant"] = np.zeros((T, H if qk == 1 else H // 2), np.uint8)  # fp4: 2 per byte
         out["scales"] = np.zeros(scales_bytes(T, H, quant, sf_layout), np.uint8)
     if "y" in outputs:
         out["y"] = np.zeros((T, H), np.float64)
@@ -237,7 +273,8 @@ def combine(expert_out, row_map, weights, *, shared=None, residual=None, gamma=N
         combined_out=_ptr(out.get("combined")), residual_out=_ptr(out.get("residual")),
         norm_out=_ptr(out.get("norm")), quant_out=_ptr(out.get("quant")),
         scales_out=_ptr(out.get("scales")), y_out=_ptr(out.get("y")),
-        expert_layout=1 if slot_major else 0)
+        expert_layout=1 if slot_major else 0, io_dtype=IO_DTYPE[io_dtype],
+        weight_dtype=WEIGHT_DTYPE[weight_dtype])
     out["status"] = lib().oracle_combine(C.byref(a))
     return out
 
@@ -261,6 +298,8 @@ def dequant(q: np.ndarray, scales: np.ndarray, T: int, H: int, quant: str,
     out = np.zeros((T, H), np.float64)
     if QUANT[quant] == 1:
         lib().oracle_dequant_mxfp8(_ptr(q), _ptr(s), T, H, LAYOUT[sf_layout], _ptr(out))
+    elif QUANT[quant] == 3:
+        lib().oracle_dequant_mxfp4(_ptr(q), _ptr(s), T, H, LAYOUT[sf_layout], _ptr(out))
     else:
         lib().oracle_dequant_nvfp4(_ptr(q), _ptr(s), T, H, LAYOUT[sf_layout],
                                    global_scale, _ptr(out))

@@ -48,6 +48,8 @@
  *     the block scale's fp32 reciprocal, q = e2m1(fp32(g*y) * fp32(1/s)),
  *     q = 0 when s == 0; element 2i in the low nibble;
  *  R10 the 128x4 swizzled scale layout of the cuBLAS block-scaling format;
+ *  R16 MXFP4 block exponent: the smallest e with amax <= 6 * 2^e, like R7;
+ *     fp16 I/O and bf16 / fp16 router weights decode exactly to fp64;
  *  R15 the slot-major layout (trtllm_moe_allreduce_fusion,
  *     moe_reduction_active_experts_token_input / moe_reduction_scale_input /
  *     moe_reduction_token_input): expert rows as [k, T, H], one per slot, the
@@ -103,6 +105,50 @@ uint16_t oracle_f64_to_bf16(double d)
     uint32_t u;
     memcpy(&u, &f, sizeof u);
     return sign | (uint16_t)(u >> 16);
+}
+
+/* IEEE binary16: s.eeeee.mmmmmmmmmm, bias 15, subnormals m * 2^-24. */
+double oracle_f16_to_f64(uint16_t h)
+{
+    int s = (h >> 15) & 1, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 31)
+        v = m ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)m, -24);
+    else
+        v = ldexp((double)(1024 + m), e - 25);
+    return s ? -v : v;
+}
+
+/* Exact value -> binary16, round to nearest, ties to even: 11 significant
+ * bits, normal exponents down to 2^-14, fixed quantum 2^-24 below that;
+ * values that round past 65504 become infinity. */
+uint16_t oracle_f64_to_f16(double d)
+{
+    if (isnan(d))
+        return 0x7E00;
+    uint16_t sign = signbit(d) ? 0x8000 : 0;
+    double a = fabs(d);
+    if (a == 0.0)
+        return sign;
+    int p;
+    frexp(a, &p);           /* a in [2^(p-1), 2^p) */
+    int q = p - 11;         /* quantum giving 11 significant bits */
+    if (q < -24)
+        q = -24;
+    double m = nearbyint(ldexp(a, -q));
+    double r = ldexp(m, q);
+    if (r > 65504.0)
+        return sign | 0x7C00;
+    /* encode the exact binary16 value r */
+    if (r < ldexp(1.0, -14))
+        return sign | (uint16_t)(r * ldexp(1.0, 24));
+    int pe;
+    double f = frexp(r, &pe); /* r = f * 2^pe, f in [0.5, 1) */
+    int e = pe - 1 + 15;
+    uint16_t man = (uint16_t)((f * 2.0 - 1.0) * 1024.0);
+    return sign | (uint16_t)(e << 10) | man;
 }
 
 /* float8 e4m3 ("fn": finite, no infinity): s.eeee.mmm, bias 7; exponent
@@ -194,6 +240,28 @@ uint8_t oracle_ue8m0_for_amax(double amax)
     return (uint8_t)b;
 }
 
+/* UE8M0 block scale for MXFP4 (reading R16): the smallest integer e with
+ * amax <= 6 * 2^e (6 is the largest e2m1 magnitude), biased by 127 and
+ * clamped to [0, 254].  amax == 0 -> 0. */
+uint8_t oracle_ue8m0_fp4_for_amax(double amax)
+{
+    if (!(amax > 0.0))
+        return 0;
+    int p;
+    frexp(amax, &p);
+    int e = p - 3;
+    while (ldexp(6.0, e) < amax)
+        e++;
+    while (ldexp(6.0, e - 1) >= amax)
+        e--;
+    int b = e + 127;
+    if (b < 0)
+        b = 0;
+    if (b > 254)
+        b = 254;
+    return (uint8_t)b;
+}
+
 /* Byte offset of scale (row r, column c) in a scale matrix of C columns.
  * layout 0: linear, row-major.  layout 1: 128x4 swizzle (reading R10):
  * 128-row x 4-column tiles of 512 bytes, tiles ordered row-tile major with
@@ -219,7 +287,7 @@ void oracle_sf_offsets(int64_t T, int64_t C, int32_t layout, int64_t *out)
 /* Size in bytes of the scale matrix for T rows and H elements per row. */
 int64_t oracle_scales_bytes(int64_t T, int32_t H, int32_t quant, int32_t layout)
 {
-    int64_t vec = (quant == 1) ? 32 : 16;
+    int64_t vec = (quant == 2) ? 16 : 32;  /* NVFP4 16; MXFP8 and MXFP4 32 */
     int64_t C = H / vec;
     if (layout == 0)
         return T * C;
@@ -306,6 +374,8 @@ typedef struct {
     int32_t expert_layout;      /* 0: rows grouped by expert, found through row_map;
                                    1: slot-major [k, T, H], row of (t, j) at j * T + t,
                                       row_map unused (reading R15) */
+    int32_t io_dtype;           /* 16-bit tensors in and out: 0 bf16, 1 fp16 */
+    int32_t weight_dtype;       /* router weights: 0 fp32, 1 bf16, 2 fp16 */
     int32_t pad0;
 } oracle_combine_args;
 
@@ -328,6 +398,31 @@ static void quant_mxfp8_row(const float *y32, int32_t H, int64_t t, int32_t layo
         scales[oracle_sf_offset(t, c, C, layout)] = b;
         for (int i = 0; i < 32; i++)
             q[c * 32 + i] = oracle_e4m3_from_f64(ldexp((double)y32[c * 32 + i], 127 - b));
+    }
+}
+
+/* MXFP4 (moe_a2a_combine: the MXFP4 path, which ignores
+ * output_scalar_scale) of one row already rounded to fp32: UE8M0 scale per
+ * 32 elements (reading R16), e2m1 codes of y * 2^-e, element 2i in the low
+ * nibble. */
+static void quant_mxfp4_row(const float *y32, int32_t H, int64_t t, int32_t layout, uint8_t *q,
+                            uint8_t *scales)
+{
+    int64_t C = H / 32;
+    for (int64_t c = 0; c < C; c++) {
+        double amax = 0.0;
+        for (int i = 0; i < 32; i++) {
+            double v = fabs((double)y32[c * 32 + i]);
+            if (v > amax)
+                amax = v;
+        }
+        uint8_t b = oracle_ue8m0_fp4_for_amax(amax);
+        scales[oracle_sf_offset(t, c, C, layout)] = b;
+        for (int i = 0; i < 32; i += 2) {
+            uint8_t lo = oracle_e2m1_from_f64(ldexp((double)y32[c * 32 + i], 127 - b));
+            uint8_t hi = oracle_e2m1_from_f64(ldexp((double)y32[c * 32 + i + 1], 127 - b));
+            q[c * 16 + i / 2] = (uint8_t)(lo | (hi << 4));
+        }
     }
 }
 
@@ -362,11 +457,34 @@ static void quant_nvfp4_row(const float *y32, int32_t H, int64_t t, int32_t layo
     }
 }
 
+/* A 16-bit input element of the combine (bf16 or fp16, io_dtype). */
+static double in16(const oracle_combine_args *a, uint16_t v)
+{
+    return a->io_dtype == 1 ? oracle_f16_to_f64(v) : oracle_bf16_to_f64(v);
+}
+
+/* A 16-bit output element (bf16 or fp16), round to nearest even. */
+static uint16_t out16(const oracle_combine_args *a, double v)
+{
+    return a->io_dtype == 1 ? oracle_f64_to_f16(v) : oracle_f64_to_bf16(v);
+}
+
+/* Router weight (t, j) as fp32 (Struct_ep_combine_skip_a2a,
+ * router_weights_dtype): stored as fp32, bf16 or fp16. */
+static double weight_at(const oracle_combine_args *a, int64_t idx)
+{
+    if (a->weight_dtype == 1)
+        return oracle_bf16_to_f64(((const uint16_t *)a->weights)[idx]);
+    if (a->weight_dtype == 2)
+        return oracle_f16_to_f64(((const uint16_t *)a->weights)[idx]);
+    return (double)a->weights[idx];
+}
+
 int oracle_combine(const oracle_combine_args *a)
 {
     if (!a || a->T < 0 || a->H < 1 || a->k < 1)
         return ORACLE_ERR_INVALID_ARG;
-    if (a->quant == 1 && a->H % 32)
+    if ((a->quant == 1 || a->quant == 3) && a->H % 32)
         return ORACLE_ERR_INVALID_ARG;
     if (a->quant == 2 && a->H % 16)
         return ORACLE_ERR_INVALID_ARG;
@@ -396,24 +514,24 @@ int oracle_combine(const oracle_combine_args *a)
                 status = ORACLE_ERR_INVALID_ARG;
                 continue;
             }
-            double w = (double)a->weights[t * k + j];
+            double w = weight_at(a, t * k + j);
             const uint16_t *row = a->expert_out + (int64_t)r * H;
             for (int32_t h = 0; h < H; h++)
-                s[h] += w * oracle_bf16_to_f64(row[h]);
+                s[h] += w * in16(a, row[h]);
         }
         /* fused shared expert, weight 1 */
         if (a->shared)
             for (int32_t h = 0; h < H; h++)
-                s[h] += oracle_bf16_to_f64(a->shared[t * H + h]);
+                s[h] += in16(a, a->shared[t * H + h]);
         if (a->combined_out)
             for (int32_t h = 0; h < H; h++)
-                a->combined_out[t * H + h] = oracle_f64_to_bf16(s[h]);
+                a->combined_out[t * H + h] = out16(a, s[h]);
         /* residual add (trtllm_moe_allreduce_fusion residual_in / residual_out) */
         for (int32_t h = 0; h < H; h++)
-            x[h] = s[h] + (a->residual ? oracle_bf16_to_f64(a->residual[t * H + h]) : 0.0);
+            x[h] = s[h] + (a->residual ? in16(a, a->residual[t * H + h]) : 0.0);
         if (a->residual_out)
             for (int32_t h = 0; h < H; h++)
-                a->residual_out[t * H + h] = oracle_f64_to_bf16(x[h]);
+                a->residual_out[t * H + h] = out16(a, x[h]);
         /* RMSNorm with weight_bias (trtllm_moe_allreduce_fusion rms_gamma,
          * rms_eps, weight_bias) */
         if (a->gamma) {
@@ -422,12 +540,12 @@ int oracle_combine(const oracle_combine_args *a)
                 ss += x[h] * x[h];
             double rinv = 1.0 / sqrt(ss / (double)H + (double)a->eps);
             for (int32_t h = 0; h < H; h++) {
-                double g = oracle_bf16_to_f64(a->gamma[h]) + (double)a->weight_bias;
+                double g = in16(a, a->gamma[h]) + (double)a->weight_bias;
                 x[h] = x[h] * rinv * g;
             }
             if (a->norm_out)
                 for (int32_t h = 0; h < H; h++)
-                    a->norm_out[t * H + h] = oracle_f64_to_bf16(x[h]);
+                    a->norm_out[t * H + h] = out16(a, x[h]);
         }
         if (a->y_out)
             for (int32_t h = 0; h < H; h++)
@@ -438,6 +556,8 @@ int oracle_combine(const oracle_combine_args *a)
                 y32[h] = (float)x[h];
             if (a->quant == 1)
                 quant_mxfp8_row(y32, H, t, a->sf_layout, a->quant_out + t * H, a->scales_out);
+            else if (a->quant == 3)
+                quant_mxfp4_row(y32, H, t, a->sf_layout, a->quant_out + t * (H / 2), a->scales_out);
             else
                 quant_nvfp4_row(y32, H, t, a->sf_layout, a->global_scale,
                                 a->quant_out + t * (H / 2), a->scales_out);
@@ -490,6 +610,20 @@ void oracle_dequant_mxfp8(const uint8_t *q, const uint8_t *scales, int64_t T, in
         for (int32_t h = 0; h < H; h++) {
             uint8_t b = scales[oracle_sf_offset(t, h / 32, C, layout)];
             out[t * H + h] = ldexp(oracle_e4m3_to_f64(q[t * H + h]), (int)b - 127);
+        }
+}
+
+/* out[t, h] = e2m1(q) * 2^(scale - 127) */
+void oracle_dequant_mxfp4(const uint8_t *q, const uint8_t *scales, int64_t T, int32_t H, int32_t layout,
+                          double *out)
+{
+    int64_t C = H / 32;
+    for (int64_t t = 0; t < T; t++)
+        for (int32_t h = 0; h < H; h++) {
+            uint8_t byte = q[t * (H / 2) + h / 2];
+            uint8_t code = (h & 1) ? (byte >> 4) : (byte & 15);
+            uint8_t b = scales[oracle_sf_offset(t, h / 32, C, layout)];
+            out[t * H + h] = ldexp(oracle_e2m1_to_f64(code), (int)b - 127);
         }
 }
 

@@ -74,7 +74,7 @@ def gpu_combine(wl, inp, d_row_map, *, global_scale=1.0, outputs=None, stream=No
         if name in outputs:
             bufs[name], views[name] = out(T * H, torch.int16)
     if wl.quant and "quant" in outputs:
-        qn = T * H if wl.quant == "mxfp8" else T * H // 2
+        qn = T * H if wl.quant == "mxfp8" else T * H // 2  # fp4: two codes per byte
         bufs["quant"], views["quant"] = out(qn, torch.uint8)
         sn = nqg.moe_scales_bytes(T, H, wl.quant, wl.sf_layout)
         bufs["scales"], views["scales"] = out(sn, torch.uint8)
@@ -84,7 +84,8 @@ def gpu_combine(wl, inp, d_row_map, *, global_scale=1.0, outputs=None, stream=No
                     quant=wl.quant, sf_layout=wl.sf_layout, global_scale=global_scale,
                     combined_out=views.get("combined"), residual_out=views.get("residual"),
                     norm_out=views.get("norm"), quant_out=views.get("quant"),
-                    scales_out=views.get("scales"), status=status, H=H, expert_layout=expert_layout)
+                    scales_out=views.get("scales"), status=status, H=H, expert_layout=expert_layout,
+                    io_dtype=wl.io_dtype, weight_dtype=wl.weight_dtype)
     torch.cuda.synchronize()
     res = {"status": int(status.item())}
     for name, v in views.items():
@@ -112,22 +113,38 @@ def oracle_combine(wl, inp, row_map, *, tokens=None, global_scale=1.0,
         return oracle.combine(
             inp["expert_out"], None, inp["weights"], shared=inp["shared"], residual=inp["residual"],
             gamma=inp["gamma"], eps=wl.eps, weight_bias=wl.weight_bias, quant=wl.quant,
-            sf_layout=sf_layout or wl.sf_layout, global_scale=global_scale, expert_layout="slot_major")
+            sf_layout=sf_layout or wl.sf_layout, global_scale=global_scale, expert_layout="slot_major",
+            io_dtype=wl.io_dtype, weight_dtype=wl.weight_dtype)
     return oracle.combine(
         inp["expert_out"], row_map[sel], inp["weights"][sel], shared=pick(inp["shared"]),
         residual=pick(inp["residual"]), gamma=inp["gamma"], eps=wl.eps,
         weight_bias=wl.weight_bias, quant=wl.quant,
         sf_layout=(sf_layout or (wl.sf_layout if tokens is None else "linear")),
-        global_scale=global_scale)
+        global_scale=global_scale, io_dtype=wl.io_dtype, weight_dtype=wl.weight_dtype)
 
 
-def bf16_ulp(x: np.ndarray) -> np.ndarray:
+def bf16_ulp(x: np.ndarray, io="bf16") -> np.ndarray:
+    """Spacing of the 16-bit output format at |x| (bf16: 8 significant bits,
+    normal down to 2^-126; fp16: 11 bits, normal down to 2^-14)."""
     a = np.abs(x)
+    if io == "fp16":
+        e = np.floor(np.log2(np.maximum(a, 2.0 ** -14)))
+        return 2.0 ** (e - 10)
     e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
     return 2.0 ** (e - 7)
 
 
-def sum_magnitude(inp, row_map, tokens) -> np.ndarray:
+def dec16(bits, io="bf16") -> np.ndarray:
+    return oracle.f16_to_f64(bits) if io == "fp16" else oracle.bf16_to_f64(bits)
+
+
+def dec_weights(w, dtype="fp32") -> np.ndarray:
+    if dtype == "fp32":
+        return np.asarray(w, np.float64)
+    return dec16(w, "fp16" if dtype == "fp16" else "bf16")
+
+
+def sum_magnitude(inp, row_map, tokens, io="bf16", weight_dtype="fp32") -> np.ndarray:
     """Per element sum of |terms| of x = sum_j w x_j + shared + residual
     (row_map None: the slot-major layout [k, T, H])."""
     tokens = np.asarray(tokens)
@@ -135,6 +152,7 @@ def sum_magnitude(inp, row_map, tokens) -> np.ndarray:
         inp["residual"].shape[1] if inp["residual"] is not None else 1)
     mag = np.zeros((tokens.size, H))
     rows = inp["expert_out"]
+    wts = dec_weights(inp["weights"], weight_dtype)
     if row_map is None:
         k, T = rows.shape[0], rows.shape[1]
         row_map = (np.arange(k)[None, :] * T + np.arange(T)[:, None]).astype(np.int32)
@@ -143,18 +161,18 @@ def sum_magnitude(inp, row_map, tokens) -> np.ndarray:
         for j in range(row_map.shape[1]):
             r = row_map[t, j]
             if r >= 0:
-                mag[i] += abs(float(inp["weights"][t, j])) * np.abs(oracle.bf16_to_f64(rows[r]))
+                mag[i] += abs(float(wts[t, j])) * np.abs(dec16(rows[r], io))
         if inp["shared"] is not None:
-            mag[i] += np.abs(oracle.bf16_to_f64(inp["shared"][t]))
+            mag[i] += np.abs(dec16(inp["shared"][t], io))
         if inp["residual"] is not None:
-            mag[i] += np.abs(oracle.bf16_to_f64(inp["residual"][t]))
+            mag[i] += np.abs(dec16(inp["residual"][t], io))
     return mag
 
 
-def assert_bf16_close(got: np.ndarray, want: np.ndarray, abs_floor, what: str):
-    g = oracle.bf16_to_f64(got)
-    w = oracle.bf16_to_f64(want)
-    tol = 2 * bf16_ulp(w) + abs_floor
+def assert_bf16_close(got: np.ndarray, want: np.ndarray, abs_floor, what: str, io="bf16"):
+    g = dec16(got, io)
+    w = dec16(want, io)
+    tol = 2 * bf16_ulp(w, io) + abs_floor
     bad = np.abs(g - w) > tol
     if bad.any():
         i = np.argwhere(bad)[:5]
@@ -168,13 +186,13 @@ def quant_step(codes_deq_scaled: np.ndarray, quant: str) -> np.ndarray:
     if quant == "mxfp8":
         e = np.floor(np.log2(np.maximum(a, 2.0 ** -6)))
         return 2.0 ** (e - 3)          # subnormal spacing 2^-9 below 2^-6
-    return np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))
+    return np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))   # e2m1 (NVFP4, MXFP4)
 
 
 def assert_quant_close(wl, got_q, got_s, want_q, want_s, T, H, global_scale, what,
                        layout=None):
     layout = layout or wl.sf_layout
-    vec = 32 if wl.quant == "mxfp8" else 16
+    vec = 16 if wl.quant == "nvfp4" else 32
     Cc = H // vec
     idx = oracle.sf_offsets(T, Cc, layout)
     gs, ws = got_s[idx], want_s[idx]
@@ -184,7 +202,7 @@ def assert_quant_close(wl, got_q, got_s, want_q, want_s, T, H, global_scale, wha
     assert np.all(np.abs(diff) <= 1), f"{what}: a scale byte differs by more than one step"
     dg = oracle.dequant(got_q, got_s, T, H, wl.quant, layout, global_scale)
     dw = oracle.dequant(want_q, want_s, T, H, wl.quant, layout, global_scale)
-    if wl.quant == "mxfp8":
+    if wl.quant in ("mxfp8", "mxfp4"):
         sc = 2.0 ** (np.maximum(gs, ws).astype(np.float64) - 127)
     else:
         sc = np.maximum(oracle.e4m3_to_f64(gs), oracle.e4m3_to_f64(ws)) / global_scale
@@ -202,6 +220,7 @@ def nvfp4_global_scale(wl, inp, row_map, expert_layout="grouped") -> float:
     """g = fp32(448 * 6 / amax(y)) over the whole tensor, from the oracle's y."""
     o = oracle.combine(inp["expert_out"], row_map, inp["weights"], shared=inp["shared"],
                        residual=inp["residual"], gamma=inp["gamma"], eps=wl.eps,
-                       weight_bias=wl.weight_bias, outputs=("y",), expert_layout=expert_layout)
+                       weight_bias=wl.weight_bias, outputs=("y",), expert_layout=expert_layout,
+                       io_dtype=wl.io_dtype, weight_dtype=wl.weight_dtype)
     amax = float(np.abs(o["y"]).max())
     return float(np.float32(448.0 * 6.0 / amax)) if amax > 0 else 1.0

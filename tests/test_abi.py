@@ -41,13 +41,14 @@ def test_every_declared_symbol_is_exported(L):
 
 def test_abi_version_and_struct(L):
     assert nqg.moe_abi_version() == nqg.ABI_VERSION
-    assert L.moe_combine_args_size() == C.sizeof(nqg.MoeCombineArgs) == 144
+    assert L.moe_combine_args_size() == C.sizeof(nqg.MoeCombineArgs) == 152
     assert nqg.moe_status_string(0) == "MOE_OK"
     assert "INVALID_EXPERT" in nqg.moe_status_string(4)
 
 
 @pytest.mark.parametrize("T,H,q,lay", [(4096, 7168, "mxfp8", "linear"), (8192, 4096, "nvfp4", "swizzled"),
                                        (1, 32, "mxfp8", "swizzled"), (130, 96, "mxfp8", "swizzled"),
+                                       (70, 64, "mxfp4", "swizzled"), (9, 96, "mxfp4", "linear"),
                                        (7, 48, "nvfp4", "linear"), (0, 64, "nvfp4", "swizzled")])
 def test_scales_bytes_match_oracle(L, T, H, q, lay):
     assert nqg.moe_scales_bytes(T, H, q, lay) == oracle.scales_bytes(T, H, q, lay)
@@ -80,6 +81,8 @@ def _args(**kw):
     (dict(norm_out=0x7000), 1), (dict(expert_out=0x1008), 1), (dict(combined_out=0x4004), 1),
     (dict(row_map=0x2002), 1), (dict(eps=-1.0), 1), (dict(eps=float("nan")), 1),
     (dict(expert_layout=2), 1), (dict(status=0x8002), 1),
+    (dict(io_dtype=2), 1), (dict(weight_dtype=3), 1), (dict(router_weights=0x3002), 1),
+    (dict(quant=3, H=48, quant_out=0x5000, scales_out=0x6000), 1),  # MXFP4 needs H % 32
     (dict(expert_layout=1, row_map=None, n_expert_rows=7), 1),  # slot-major needs top_k * T rows
     (dict(T=0), 0),  # a valid no-op: returns before any CUDA call
     (dict(T=0, row_map=None, router_weights=None, expert_out=None, combined_out=None), 0),

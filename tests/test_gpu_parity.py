@@ -17,7 +17,7 @@ import oracle
 from norm_quant_gb300 import synth
 from norm_quant_gb300.build import build
 
-from _helpers import (assert_bf16_close, assert_quant_close, d, gpu_combine, gpu_route, h,
+from _helpers import (assert_bf16_close, assert_quant_close, d, dec16, gpu_combine, gpu_route, h,
                       nvfp4_global_scale, oracle_combine, sum_magnitude)
 
 pytestmark = pytest.mark.gpu
@@ -48,19 +48,20 @@ def compare(wl, inp, orm, got, tokens=None, global_scale=1.0, expert_layout="gro
     o = oracle_combine(wl, inp, orm, tokens=None if tokens is None else tok, global_scale=global_scale,
                        expert_layout=expert_layout)
     assert o["status"] == 0
-    mag = sum_magnitude(inp, orm, tok)
+    io = wl.io_dtype
+    mag = sum_magnitude(inp, orm, tok, io, wl.weight_dtype)
     floor = GAMMA_K(k) * mag
     for name in ("combined", "residual"):
         if name in got:
-            assert_bf16_close(got[name][tok], o[name], floor, f"{wl.name}:{name}")
+            assert_bf16_close(got[name][tok], o[name], floor, f"{wl.name}:{name}", io)
     if "norm" in got:
-        res = oracle.bf16_to_f64(o["residual"])
+        res = dec16(o["residual"], io)
         rinv = 1.0 / np.sqrt((res ** 2).mean(axis=1, keepdims=True) + wl.eps)
-        g = np.abs(oracle.bf16_to_f64(inp["gamma"]) + wl.weight_bias)[None, :]
+        g = np.abs(dec16(inp["gamma"], io) + wl.weight_bias)[None, :]
         nfloor = 2 * floor * rinv * g + 2.0 ** -20 * np.abs(o["y"])
-        assert_bf16_close(got["norm"][tok], o["norm"], nfloor, f"{wl.name}:norm")
+        assert_bf16_close(got["norm"][tok], o["norm"], nfloor, f"{wl.name}:norm", io)
     if wl.quant and "quant" in got:
-        vec = 32 if wl.quant == "mxfp8" else 16
+        vec = 16 if wl.quant == "nvfp4" else 32
         Cc = H // vec
         if tokens is None:
             assert_quant_close(wl, got["quant"], got["scales"], o["quant"], o["scales"], T, H,
@@ -279,3 +280,30 @@ def test_dispatch_permute_reports_out_of_range_rows():
     assert int(status.item()) == nqg.MOE_ERR_ROW_OUT_OF_RANGE
     st, want = oracle.dispatch_permute(x, rm, T * k)
     assert np.array_equal(h(xg, np.uint16), want)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(T=300, H=7168, k=8, E=64, shared_std=0.5, quant="mxfp4", outputs=("residual", "quant")),
+    dict(T=130, H=96, k=4, quant="mxfp4", sf_layout="swizzled", outputs=("norm", "quant")),
+    dict(T=200, H=4096, k=8, E=128, gamma_mean=0.0, weight_bias=1.0, quant="mxfp4", sf_layout="swizzled",
+         outputs=("residual", "quant")),
+    dict(T=257, H=7168, k=8, E=256, shared_std=0.5, io_dtype="fp16",
+         outputs=("combined", "residual", "norm")),
+    dict(T=257, H=4096, k=8, E=128, io_dtype="fp16", gamma_mean=0.0, weight_bias=1.0, quant="nvfp4",
+         sf_layout="swizzled", outputs=("residual", "quant")),
+    dict(T=300, H=7168, k=8, E=256, shared_std=0.5, weight_dtype="bf16", quant="mxfp8",
+         outputs=("residual", "quant")),
+    dict(T=100, H=2048, k=6, E=32, weight_dtype="fp16", io_dtype="fp16", quant="mxfp4",
+         outputs=("combined", "norm", "quant")),
+], ids=["mxfp4_prefill_like", "mxfp4_swizzled_pad", "mxfp4_gemma_like", "fp16_io_norm",
+        "fp16_io_nvfp4", "bf16_weights_mxfp8", "fp16_weights_fp16_io_mxfp4"])
+def test_dtype_and_mxfp4_parity(kw):
+    """MXFP4 output (UE8M0 per 32, e2m1 codes), fp16 inputs and outputs, and
+    bf16 / fp16 router weights, against the oracle."""
+    wl = _wl(**kw)
+    inp = synth.make_inputs(wl)
+    d_rm, orm = route_and_check(inp["topk_ids"], wl.E)
+    g = nvfp4_global_scale(wl, inp, orm) if wl.quant == "nvfp4" else 1.0
+    got = gpu_combine(wl, inp, d_rm, global_scale=g, canary=True)
+    assert got["status"] == 0
+    compare(wl, inp, orm, got, global_scale=g)

@@ -340,3 +340,57 @@ def test_slot_major_one_hot_recovers_slot_and_token():
         for j in range(k):
             want[t, j * T + t] = w[t, j]
     assert np.array_equal(f(o["combined"]), want)
+
+
+# --------------------------------------------------------- dtype variants --
+
+def test_mxfp4_grid_values_roundtrip_exactly():
+    H, T = 96, 5
+    fp4 = oracle.e2m1_to_f64(np.arange(8, dtype=np.uint8))
+    rows, codes, scales = [], [], []
+    for t in range(T):
+        for blk in range(H // 32):
+            e = int(RNG.integers(-12, 12))
+            c = RNG.integers(0, 8, 32).astype(np.uint8)
+            c[RNG.integers(0, 32)] = 7                          # amax = 6 * 2^e
+            c = c | (RNG.integers(0, 2, 32).astype(np.uint8) << 3)
+            rows.append(np.where(c & 8, -1.0, 1.0) * fp4[c & 7] * 2.0 ** e)
+            codes.append(c)
+            scales.append(e + 127)
+    rows = np.concatenate(rows).reshape(T, H)
+    o = oracle.combine(bf(rows), np.arange(T, dtype=np.int32)[:, None], np.ones((T, 1), np.float32),
+                       quant="mxfp4")
+    assert o["scales"].tolist() == scales
+    got = np.stack([o["quant"] & 15, o["quant"] >> 4], axis=-1).reshape(T, H)
+    c = np.concatenate(codes).reshape(T, H)
+    nz = (c & 7) != 0
+    assert np.array_equal(got[nz], c[nz]) and np.all((got[~nz] & 7) == 0)
+    assert np.array_equal(oracle.dequant(o["quant"], o["scales"], T, H, "mxfp4"), rows)
+
+
+def test_low_precision_weights_equal_their_fp32_values():
+    T, k, E, H = 20, 4, 8, 64
+    ids, row_map, nv = _routing(T, k, E)
+    rows = bf(RNG.standard_normal((nv, H)))
+    w32 = np.array(RNG.dirichlet(np.ones(k), T), np.float32)
+    for name, enc, dec in (("bf16", bf, f), ("fp16", oracle.f64_to_f16, oracle.f16_to_f64)):
+        wbits = enc(w32)
+        a = oracle.combine(rows, row_map, wbits, weight_dtype=name, quant="mxfp8")
+        b = oracle.combine(rows, row_map, dec(wbits).astype(np.float32), quant="mxfp8")
+        for key in ("combined", "y", "quant", "scales"):
+            assert np.array_equal(a[key], b[key]), (name, key)
+
+
+def test_fp16_io_agrees_with_bf16_on_values_both_hold_exactly():
+    # small dyadic values are exact in both formats and so are their sums,
+    # so the fp16 and bf16 paths must produce the same numbers
+    T, k, E, H = 12, 3, 6, 32
+    ids, row_map, nv = _routing(T, k, E)
+    vals = RNG.integers(-16, 17, (nv, H)) / 8.0
+    w = (2.0 ** -RNG.integers(0, 3, (T, k))).astype(np.float32)
+    res = RNG.integers(-8, 9, (T, H)) / 4.0
+    ob = oracle.combine(bf(vals), row_map, w, residual=bf(res), outputs=("combined", "residual"))
+    oh = oracle.combine(oracle.f64_to_f16(vals), row_map, w, residual=oracle.f64_to_f16(res),
+                        outputs=("combined", "residual"), io_dtype="fp16")
+    for key in ("combined", "residual"):
+        assert np.array_equal(f(ob[key]), oracle.f16_to_f64(oh[key])), key

@@ -217,3 +217,47 @@ def test_linear_offset_and_sizes():
     assert oracle.scales_bytes(4096, 7168, "mxfp8", "linear") == 4096 * 224
     assert oracle.scales_bytes(8192, 4096, "nvfp4", "swizzled") == 8192 * 256
     assert oracle.scales_bytes(1, 32, "mxfp8", "swizzled") == 128 * 4
+
+
+# ------------------------------------------------------------------ fp16 --
+
+def test_fp16_decode_all_codes_match_torch():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    want = torch.from_numpy(bits.view(np.int16)).view(torch.float16).double().numpy()
+    got = oracle.f16_to_f64(bits)
+    nan = np.isnan(want)
+    assert np.array_equal(nan, np.isnan(got)) and np.array_equal(got[~nan], want[~nan])
+
+
+def test_fp16_encode_matches_torch():
+    vals = torch.arange(0, 0x7C00, dtype=torch.int32).to(torch.int16).view(torch.float16).double().numpy()
+    mids = (vals[:-1] + vals[1:]) / 2
+    x = np.concatenate([vals, mids, -mids, RNG.standard_normal(4000) * 10.0 ** RNG.integers(-8, 5, 4000),
+                        [65504.0, 65519.0, 65520.0, 70000.0, 2.0 ** -25, 3 * 2.0 ** -26]])
+    x32 = x.astype(np.float32)   # torch converts float32 -> float16 with one rounding
+    want = torch.from_numpy(x32).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.f64_to_f16(x32.astype(np.float64))
+    assert np.array_equal(got, want)
+
+
+# --------------------------------------------------------- MXFP4 scale rule --
+
+def _ue8m0_fp4_brute(amax: float) -> int:
+    if amax == 0:
+        return 0
+    a = Fraction(amax)
+    e = -200
+    while Fraction(6) * Fraction(2) ** e < a:
+        e += 1
+    return max(0, min(254, e + 127))
+
+
+def test_ue8m0_fp4_rule_exact():
+    f32 = np.float32
+    cases = [0.0, 6.0, 3.0, 1.5, 1.5000001, 12.0, 0.75, 1e-30, 1e30]
+    for e in range(-20, 20):
+        b = 6.0 * 2.0 ** e
+        cases += [b, float(np.nextafter(f32(b), f32(0))), float(np.nextafter(f32(b), f32(np.inf)))]
+    cases += list(np.abs(RNG.standard_normal(300)) * 10.0 ** RNG.integers(-8, 8, 300))
+    cases = [float(f32(c)) for c in cases]
+    assert oracle.ue8m0_fp4_for_amax(np.array(cases)).tolist() == [_ue8m0_fp4_brute(c) for c in cases]
