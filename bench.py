@@ -32,6 +32,7 @@ import re
 import subprocess
 import sys
 import time
+import types
 
 import numpy as np
 
@@ -41,7 +42,8 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE combine tokens/s and achieved HBM GB/s vs peak (T=4096,H=7168,k=8)"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_SOURCES = ["norm_quant_gb300/csrc/combine.cu", "norm_quant_gb300/csrc/ptx.cuh"]
+KERNEL_SOURCES = ["norm_quant_gb300/csrc/combine.cu", "norm_quant_gb300/csrc/combine_impl.cuh",
+                  "norm_quant_gb300/csrc/ptx.cuh"]
 TRAFFIC_FILE = "profiles/combine_prefill_T4096_H7168_k8_mxfp8.md"
 
 
@@ -51,7 +53,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", choices=["tiny", "decode", "prefill", "gemma", "padded",
@@ -279,50 +281,60 @@ def run_ours(args):
     names = [n for n in ("topk_ids", "weights", "expert_out", "shared", "residual", "gamma", "x")
              if inp.get(n) is not None]
     host = {n: pinned(inp[n]) for n in names}
-    dv = {n: t.to(dev) for n, t in host.items()}
-    counts = torch.empty(E, dtype=torch.int32, device=dev)
-    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
-    row_map = torch.empty((T, k), dtype=torch.int32, device=dev)
-    ws = torch.empty(nqg.moe_build_row_map_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
-    outs = {}
-    if kind == "dispatch":
-        outs["x_grouped"] = torch.empty((inp["n_valid"], H), dtype=torch.int16, device=dev)
-    for o in ("combined", "residual", "norm"):
-        if kind != "dispatch" and o in wl.outputs:
-            outs[o] = torch.empty((T, H), dtype=torch.int16, device=dev)
-    if kind != "dispatch" and wl.quant:
-        outs["quant"] = torch.empty((T, H if wl.quant == "mxfp8" else H // 2), dtype=torch.uint8, device=dev)
-        outs["scales"] = torch.empty(nqg.moe_scales_bytes(T, H, wl.quant, wl.sf_layout), dtype=torch.uint8,
-                                     device=dev)
     flush = torch.empty(L2_FLUSH_BYTES if args.l2 == "write" else 16, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    args_c = None
-    if kind != "dispatch":
-        # NVFP4's per-tensor scale only changes which codes come out, not the work
-        args_c = nqg.combine_args(expert_out=dv["expert_out"].reshape(-1, H),
-                                  row_map=None if kind == "slot_major" else row_map,
-                                  router_weights=dv["weights"], shared_out=dv.get("shared"),
-                                  residual=dv.get("residual"), gamma=dv.get("gamma"), eps=wl.eps,
-                                  weight_bias=wl.weight_bias, quant=wl.quant, sf_layout=wl.sf_layout,
-                                  global_scale=1.0, combined_out=outs.get("combined"),
-                                  residual_out=outs.get("residual"), norm_out=outs.get("norm"),
-                                  quant_out=outs.get("quant"), scales_out=outs.get("scales"), H=H,
-                                  expert_layout="slot_major" if kind == "slot_major" else "grouped")
     route_kernels = 0 if kind == "slot_major" else (1 if (T * k <= 524288 and E <= 1024) else 3)
 
-    def route(st):
-        if kind != "slot_major":
-            nqg.moe_build_row_map(dv["topk_ids"], E, counts, offsets, row_map, None, ws, stream=st)
-
-    def combine(st):  # the dominant kernel of the step
+    def buffer_set():
+        """Device inputs, outputs and the calls of one step over them."""
+        b = types.SimpleNamespace()
+        b.dv = {n: t.to(dev) for n, t in host.items()}
+        b.counts = torch.empty(E, dtype=torch.int32, device=dev)
+        b.offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        b.row_map = torch.empty((T, k), dtype=torch.int32, device=dev)
+        b.ws = torch.empty(nqg.moe_build_row_map_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
+        b.outs = {}
         if kind == "dispatch":
-            nqg.moe_dispatch_permute(dv["x"], row_map, outs["x_grouped"], stream=st)
-        else:
-            nqg.moe_combine(stream=st, args=args_c)
+            b.outs["x_grouped"] = torch.empty((inp["n_valid"], H), dtype=torch.int16, device=dev)
+        for o in ("combined", "residual", "norm"):
+            if kind != "dispatch" and o in wl.outputs:
+                b.outs[o] = torch.empty((T, H), dtype=torch.int16, device=dev)
+        if kind != "dispatch" and wl.quant:
+            b.outs["quant"] = torch.empty((T, H if wl.quant == "mxfp8" else H // 2), dtype=torch.uint8,
+                                          device=dev)
+            b.outs["scales"] = torch.empty(nqg.moe_scales_bytes(T, H, wl.quant, wl.sf_layout),
+                                           dtype=torch.uint8, device=dev)
+        b.args_c = None
+        if kind != "dispatch":
+            # NVFP4's per-tensor scale only changes which codes come out, not the work
+            b.args_c = nqg.combine_args(
+                expert_out=b.dv["expert_out"].reshape(-1, H), row_map=None if kind == "slot_major" else b.row_map,
+                router_weights=b.dv["weights"], shared_out=b.dv.get("shared"), residual=b.dv.get("residual"),
+                gamma=b.dv.get("gamma"), eps=wl.eps, weight_bias=wl.weight_bias, quant=wl.quant,
+                sf_layout=wl.sf_layout, global_scale=1.0, combined_out=b.outs.get("combined"),
+                residual_out=b.outs.get("residual"), norm_out=b.outs.get("norm"), quant_out=b.outs.get("quant"),
+                scales_out=b.outs.get("scales"), H=H,
+                expert_layout="slot_major" if kind == "slot_major" else "grouped")
 
-    def step(st):
-        route(st)
-        combine(st)
+        def route(st):
+            if kind != "slot_major":
+                nqg.moe_build_row_map(b.dv["topk_ids"], E, b.counts, b.offsets, b.row_map, None, b.ws, stream=st)
+
+        def combine(st):  # the dominant kernel of the step
+            if kind == "dispatch":
+                nqg.moe_dispatch_permute(b.dv["x"], b.row_map, b.outs["x_grouped"], stream=st)
+            else:
+                nqg.moe_combine(stream=st, args=b.args_c)
+
+        def step(st):
+            route(st)
+            combine(st)
+
+        b.route, b.combine, b.step = route, combine, step
+        return b
+
+    bufs = [buffer_set()]
+    route, combine, step, ws = bufs[0].route, bufs[0].combine, bufs[0].step, bufs[0].ws
 
     gs = torch.cuda.Stream(dev)
     with torch.cuda.stream(gs):
@@ -376,28 +388,51 @@ def run_ours(args):
         comb_s = replay(g_comb, K) / K         # the combine kernel alone, same count
     total_s = max_over_ranks(total_s, dev)
 
-    # end to end through the C ABI from pinned host buffers
-    host_out = {n: torch.empty_like(t, device="cpu").pin_memory() for n, t in outs.items()}
+    # end to end through the C ABI from pinned host buffers: every step copies
+    # its inputs in and its outputs out.  Two buffer sets and three streams
+    # (copy-in, compute, copy-out) overlap step i + 1's copy-in with step i's
+    # compute and copy-out, as a serving loop would; the timed region runs
+    # from the first copy-in to the last copy-out.
+    bufs.append(buffer_set())
+    host_out = [{n: torch.empty_like(t, device="cpu").pin_memory() for n, t in b.outs.items()} for b in bufs]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
+    s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    freed = [ev(), ev()]      # a set's inputs were consumed by its last compute
+    drained = [ev(), ev()]    # a set's outputs were copied out
 
-    def e2e_step():
-        for n, t in host.items():
-            dv[n].copy_(t, non_blocking=True)
-        step(stream.cuda_stream)
-        for n, t in outs.items():
-            host_out[n].copy_(t, non_blocking=True)
+    def e2e_steps(n):
+        for i in range(n):
+            b, j = bufs[i % 2], i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(freed[j])
+                for name, t in host.items():
+                    b.dv[name].copy_(t, non_blocking=True)
+                loaded = ev()
+                loaded.record(s_in)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(loaded)
+                if i >= 2:
+                    s_comp.wait_event(drained[j])
+                b.step(s_comp.cuda_stream)
+                freed[j].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(freed[j])
+                for name, t in b.outs.items():
+                    host_out[j][name].copy_(t, non_blocking=True)
+                drained[j].record(s_out)
 
-    for _ in range(2):
-        e2e_step()
+    e2e_steps(2)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(s_in)
+    e2e_steps(args.e2e_steps)
+    s_in.wait_stream(s_out)
+    t1.record(s_in)
     torch.cuda.synchronize()
-    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
+    e2e_s = max_over_ranks(t0.elapsed_time(t1) / 1e3, dev)
 
     if rank == 0:
         if kind == "dispatch":
