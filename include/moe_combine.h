@@ -56,7 +56,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 3
+#define MOE_ABI_VERSION 4
 
 /* Limits of this implementation (validated on the host). */
 #define MOE_MAX_TOP_K 32
@@ -275,12 +275,19 @@ moe_status moe_combine(const moe_combine_args *args, moe_stream_t stream);
  *   ctas_per_sm    resident CTAs per SM the grid is sized for, 1..4;
  *   route_cluster  routing build: 0 automatic, -1 the three-kernel path,
  *                  1..16 the largest thread-block cluster its single-launch
- *                  path may use.
+ *                  path may use;
+ *   combine_split  CTAs that share one token's row, as a thread-block
+ *                  cluster that splits the columns: 0 automatic (split only
+ *                  when T is below the SM count), 1 never, 2, 4, 8 or 16
+ *                  always where H allows it (slices of equal width holding
+ *                  whole quant blocks, at most 4096 columns each; otherwise
+ *                  whole rows).  vpt, rows_per_slot and ctas_per_sm apply
+ *                  to whole rows only.
  * Not synchronised with calls in flight on other host threads.  Returns
  * MOE_OK or MOE_ERR_INVALID_ARG.  (No counterpart on the pages: a tuning
  * hook of this implementation.) */
 moe_status moe_tuning_set(int32_t vpt, int32_t rows_per_slot, int32_t ring_kib, int32_t ctas_per_sm,
-                          int32_t route_cluster);
+                          int32_t route_cluster, int32_t combine_split);
 
 /* ------------------------------------------------------------------------
  * Dispatch-side permute: the step before the expert computation, the

@@ -29,7 +29,7 @@ MOE_ERR_INVALID_EXPERT = 4
 MOE_ERR_CUDA = 5
 MOE_ERR_ROW_OUT_OF_RANGE = 6
 MOE_ERR_DEVICE_TIMEOUT = 7
-ABI_VERSION = 3
+ABI_VERSION = 4
 
 
 class MoeCombineArgs(C.Structure):
@@ -73,7 +73,7 @@ SYMBOLS = {
     "moe_combine": (C.c_int, [C.POINTER(MoeCombineArgs), C.c_void_p]),
     "moe_scales_bytes": (C.c_int, [C.c_int64, C.c_int32, C.c_int32, C.c_int32,
                                    C.POINTER(C.c_size_t)]),
-    "moe_tuning_set": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
+    "moe_tuning_set": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
     "moe_dispatch_permute": (C.c_int, [C.c_void_p, C.c_int64, C.c_int32, C.c_void_p, C.c_int32,
                                        C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p]),
 }
@@ -181,9 +181,10 @@ def moe_dispatch_permute(x, row_map, x_grouped, status=None, stream=None) -> Non
 
 
 def moe_tuning_set(vpt: int = 0, rows_per_slot: int = 0, ring_kib: int = 0, ctas_per_sm: int = 0,
-                   route_cluster: int = 0) -> None:
+                   route_cluster: int = 0, combine_split: int = 0) -> None:
     """Overrides the launch plans (0 = automatic); results do not depend on it."""
-    _check(lib().moe_tuning_set(vpt, rows_per_slot, ring_kib, ctas_per_sm, route_cluster), "moe_tuning_set")
+    _check(lib().moe_tuning_set(vpt, rows_per_slot, ring_kib, ctas_per_sm, route_cluster, combine_split),
+           "moe_tuning_set")
 
 
 def combine_args(*, expert_out, row_map, router_weights, shared_out=None, residual=None,

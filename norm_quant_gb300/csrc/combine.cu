@@ -34,9 +34,15 @@
 //     row order, and release the slot on its "empty" mbarrier;
 //   * after a token's last slot: bf16 stores, a sum of squares reduced by
 //     warp shuffles and an mbarrier-synchronised cross-warp sum, the norm,
-//     and the block quantiser (an MXFP8 block is 4 consecutive lanes, NVFP4 2).
+//     and the block quantiser (an MXFP8 block is 4 consecutive lanes, NVFP4 2);
+//   * with fewer tokens than SMs, a token is split by columns over a
+//     thread-block cluster of 2..16 CTAs (each copies, sums, normalises and
+//     quantises its own slice of every row); the slices' sums of squares
+//     meet through distributed shared memory: each warp stores its partial
+//     into every CTA of the cluster and arrives on that CTA's mbarrier, and
+//     each CTA adds the partials in one fixed order.
 // Every wait is bounded (kWaitLimitNs); a wait that gives up records
-// MOE_ERR_DEVICE_TIMEOUT and the CTA drains its own copies and returns.
+// MOE_ERR_DEVICE_TIMEOUT and the CTA drains its own copies and finishes.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -59,20 +65,24 @@ using namespace nqg::combine_detail;
 
 
 extern "C" moe_status moe_tuning_set(int32_t vpt, int32_t rows_per_slot, int32_t ring_kib, int32_t ctas_per_sm,
-                                     int32_t route_cluster)
+                                     int32_t route_cluster, int32_t combine_split)
 {
     if (route_cluster < -1 || route_cluster > 16)
         return MOE_ERR_INVALID_ARG;
-    nqg::set_route_cluster(route_cluster);
     if (!(vpt == 0 || vpt == 1 || vpt == 2 || vpt == 4 || vpt == 8))
         return MOE_ERR_INVALID_ARG;
     if (rows_per_slot < 0 || rows_per_slot > 4 || ring_kib < 0 || ring_kib > 224 || ctas_per_sm < 0 ||
         ctas_per_sm > 4)
         return MOE_ERR_INVALID_ARG;
+    if (!(combine_split == 0 || combine_split == 1 || combine_split == 2 || combine_split == 4 ||
+          combine_split == 8 || combine_split == 16))
+        return MOE_ERR_INVALID_ARG;
+    nqg::set_route_cluster(route_cluster);
     g_tuning.vpt = vpt;
     g_tuning.rows = rows_per_slot;
     g_tuning.ring_kib = ring_kib;
     g_tuning.ctas_per_sm = ctas_per_sm;
+    g_tuning.split = combine_split;
     return MOE_OK;
 }
 
@@ -157,9 +167,17 @@ extern "C" moe_status moe_combine(const moe_combine_args *a, moe_stream_t stream
         p.sf_cols_pad = a->sf_layout == MOE_SF_LINEAR ? p.sf_cols : (p.sf_cols + 3) / 4 * 4;
         p.sf_rows_pad = a->sf_layout == MOE_SF_LINEAR ? p.T : (p.T + 127) / 128 * 128;
     }
-    const Plan pl = make_plan(a->H);
-    p.stages = pl.stages;
-    p.rows = pl.rows;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return a->io_dtype == MOE_IO_FP16 ? launch_io<1>(p, pl, a->quant, s) : launch_io<0>(p, pl, a->quant, s);
+    auto launch = [&](const Plan &pl) {
+        p.stages = pl.stages;
+        p.rows = pl.rows;
+        p.split = pl.split;
+        p.hl = pl.hl;
+        return a->io_dtype == MOE_IO_FP16 ? launch_io<1>(p, pl, a->quant, s) : launch_io<0>(p, pl, a->quant, s);
+    };
+    const Plan pl = make_plan(a->H, a->T, a->top_k, a->quant, g_tuning.split);
+    const moe_status st = launch(pl);
+    if (st == MOE_ERR_UNSUPPORTED && pl.split > 1)
+        return launch(make_plan(a->H, a->T, a->top_k, a->quant, 1));  // no room for the cluster: whole rows
+    return st;
 }

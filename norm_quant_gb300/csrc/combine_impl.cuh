@@ -56,6 +56,8 @@ struct Params {
     int32_t *status;
     int32_t stages, rows;  // ring slots, rows per slot
     int32_t slot_major;    // expert_out is [k, T, H]: row of (t, j) is j * T + t
+    int32_t split;         // CTAs sharing one token (the cluster size), 1 = a whole row per CTA
+    int32_t hl;            // columns each CTA handles: H / split
     int64_t sf_cols, sf_cols_pad, sf_rows_pad;
 };
 
@@ -63,15 +65,20 @@ struct SmemLayout {
     uint32_t row_stride, slot_stride, bars, meta, red, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int32_t H, int32_t stages, int32_t rows, int32_t ncw)
+// Shared memory of one CTA handling Hl columns of each row: the ring, its
+// barriers (full[S], empty[S], the cross-warp reduction barrier, a pad, and
+// the two cross-CTA reduction barriers of a split token), the slots'
+// StageMeta, then two buffers of per-warp partial sums for csize CTAs.
+__host__ __device__ inline SmemLayout smem_layout(int32_t Hl, int32_t stages, int32_t rows, int32_t ncw,
+                                                  int32_t csize)
 {
     SmemLayout L;
-    L.row_stride = (static_cast<uint32_t>(H) * 2u + 127u) & ~127u;
+    L.row_stride = (static_cast<uint32_t>(Hl) * 2u + 127u) & ~127u;
     L.slot_stride = L.row_stride * static_cast<uint32_t>(rows);
     L.bars = static_cast<uint32_t>(stages) * L.slot_stride;
-    L.meta = L.bars + (2u * stages + 2u) * 8u;  // full[S], empty[S], reduction barrier, pad
+    L.meta = L.bars + (2u * stages + 4u) * 8u;
     L.red = L.meta + static_cast<uint32_t>(stages) * static_cast<uint32_t>(sizeof(StageMeta));
-    L.total = L.red + 2u * static_cast<uint32_t>(ncw) * 4u;
+    L.total = L.red + 2u * static_cast<uint32_t>(csize) * static_cast<uint32_t>(ncw) * 4u;
     return L;
 }
 
@@ -163,7 +170,7 @@ __device__ __forceinline__ int32_t ue8m0_fp4_byte(float amax)
     return b < 0 ? 0 : (b > 254 ? 254 : b);
 }
 
-template <int VPT, int QUANT, int IO>
+template <int VPT, int QUANT, int IO, bool SPLIT>
 __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combine_kernel(const Params p)
 {
     constexpr int RMAX = max_rows<VPT>();
@@ -174,11 +181,25 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
     const int S = p.stages;
     const int R = p.rows;
     const int32_t H = p.H, k = p.k;
-    const int32_t nvec = H >> 3;
-    const uint32_t row_bytes = static_cast<uint32_t>(H) * 2u;
-    const SmemLayout L = smem_layout(H, S, R, ncw);
+    // This CTA handles columns [col0, col0 + Hl) of its tokens' rows: the
+    // whole row, or with SPLIT the slice of its rank in a cluster of
+    // p.split CTAs that all walk the same tokens (one token per cluster).
+    const uint32_t csize = SPLIT ? static_cast<uint32_t>(p.split) : 1u;
+    // work units (tokens in flight at once): CTAs, or with SPLIT clusters
+    const uint32_t crank = SPLIT ? cluster_rank() : 0u;
+    const int64_t unit0 = SPLIT ? cluster_id_x() : blockIdx.x;
+    auto nunits = []() -> int64_t { return SPLIT ? cluster_count_x() : gridDim.x; };
+    const int32_t Hl = SPLIT ? p.hl : H;
+    const int32_t col0 = SPLIT ? static_cast<int32_t>(crank) * Hl : 0;
+    const int32_t vec0 = col0 >> 3;  // first 8-element vector of the slice
+    const int32_t nvec = Hl >> 3;
+    const uint32_t row_bytes = static_cast<uint32_t>(H) * 2u;  // pitch of every input row
+    const uint32_t copy_bytes = static_cast<uint32_t>(Hl) * 2u;
+    const uint32_t col_bytes = static_cast<uint32_t>(col0) * 2u;
+    const SmemLayout L = smem_layout(Hl, S, R, ncw, static_cast<int32_t>(csize));
     const uint32_t ring = smem_u32(smem);
     const uint32_t full0 = ring + L.bars, empty0 = full0 + 8u * S, redbar = empty0 + 8u * S;
+    const uint32_t xbar0 = redbar + 16u;  // two cross-CTA barriers, by token parity
     StageMeta *meta = reinterpret_cast<StageMeta *>(smem + L.meta);
     float *red = reinterpret_cast<float *>(smem + L.red);
 
@@ -188,397 +209,492 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
             mbar_init(empty0 + 8u * s, ncw);
         }
         mbar_init(redbar, ncw);
+        if constexpr (SPLIT) {
+            mbar_init(xbar0, csize * ncw);
+            mbar_init(xbar0 + 8u, csize * ncw);
+        }
         fence_mbar_init();
     }
-    __syncthreads();
+    // with SPLIT, every CTA's barriers are initialised before any peer arrives on them
+    if constexpr (SPLIT)
+        cluster_arrive_wait();
+    else
+        __syncthreads();
     // launched as a programmatic dependent: nothing before this line touches
     // global memory, so the setup above overlaps the previous kernel's tail
     grid_dependency_wait();
 
     if (warp == ncw) {
         // ------------------------------------------------------- producer
-        int stage = 0;
-        uint32_t phase = 0;
-        int64_t issued = 0;
-        bool ok = true;
-        int64_t t = blockIdx.x;
-        int32_t r_next = -1;
-        float w_next = 0.f;
-        auto row_of = [&](int64_t tt) {
-            return p.slot_major ? static_cast<int32_t>(lane * p.T + tt) : __ldg(p.row_map + tt * k + lane);
-        };
-        if (t < p.T && lane < k) {
-            r_next = row_of(t);
-            w_next = load_weight(p.weights, t * k + lane, p.weight_dtype);
-        }
-        for (; t < p.T && ok; t += gridDim.x) {
-            const int32_t r = r_next;
-            const float w = w_next;
-            const int64_t tn = t + gridDim.x;
-            if (tn < p.T && lane < k) {
-                r_next = row_of(tn);
-                w_next = load_weight(p.weights, tn * k + lane, p.weight_dtype);
+        [&]() {
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            int64_t t = unit0;
+            int32_t r_next = -1;
+            float w_next = 0.f;
+            auto row_of = [&](int64_t tt) {
+                return p.slot_major ? static_cast<int32_t>(lane * p.T + tt) : __ldg(p.row_map + tt * k + lane);
+            };
+            if (t < p.T && lane < k) {
+                r_next = row_of(t);
+                w_next = load_weight(p.weights, t * k + lane, p.weight_dtype);
             }
-            bool valid = lane < k && r >= 0;
-            if (valid && r >= p.n_rows) {
-                report(p.status, MOE_ERR_ROW_OUT_OF_RANGE);
-                valid = false;
-            }
-            uint32_t mrem = __ballot_sync(0xffffffffu, valid);
-            const int n_exp = __popc(mrem);
-            const bool has_sh = p.shared != nullptr, has_res = p.residual != nullptr;
-            const int n = n_exp + (has_sh ? 1 : 0) + (has_res ? 1 : 0);
-            int i = 0;
-            do {  // one ring slot per iteration; a token with no rows still gets one
-                const int ns = (n - i < R) ? n - i : R;
-                const uint8_t *src[RMAX];
-                float wt[RMAX];
+            for (; t < p.T && ok; t += nunits()) {
+                const int32_t r = r_next;
+                const float w = w_next;
+                const int64_t tn = t + nunits();
+                if (tn < p.T && lane < k) {
+                    r_next = row_of(tn);
+                    w_next = load_weight(p.weights, tn * k + lane, p.weight_dtype);
+                }
+                bool valid = lane < k && r >= 0;
+                if (valid && r >= p.n_rows) {
+                    report(p.status, MOE_ERR_ROW_OUT_OF_RANGE);
+                    valid = false;
+                }
+                uint32_t mrem = __ballot_sync(0xffffffffu, valid);
+                const int n_exp = __popc(mrem);
+                const bool has_sh = p.shared != nullptr, has_res = p.residual != nullptr;
+                const int n = n_exp + (has_sh ? 1 : 0) + (has_res ? 1 : 0);
+                int i = 0;
+                do {  // one ring slot per iteration; a token with no rows still gets one
+                    const int ns = (n - i < R) ? n - i : R;
+                    const uint8_t *src[RMAX];
+                    float wt[RMAX];
 #pragma unroll
-                for (int q = 0; q < RMAX; ++q) {
-                    src[q] = nullptr;
-                    wt[q] = 1.f;
-                    const int ii = i + q;
-                    if (q < ns) {  // warp-uniform
-                        if (ii < n_exp) {
-                            const int j = __ffs(mrem) - 1;
-                            mrem &= mrem - 1;
-                            const int32_t rj = __shfl_sync(0xffffffffu, r, j);
-                            wt[q] = __shfl_sync(0xffffffffu, w, j);
-                            src[q] = p.expert_out + static_cast<int64_t>(rj) * row_bytes;
-                        } else if (has_sh && ii == n_exp) {
-                            src[q] = p.shared + t * row_bytes;
-                        } else {
-                            src[q] = p.residual + t * row_bytes;
+                    for (int q = 0; q < RMAX; ++q) {
+                        src[q] = nullptr;
+                        wt[q] = 1.f;
+                        const int ii = i + q;
+                        if (q < ns) {  // warp-uniform
+                            if (ii < n_exp) {
+                                const int j = __ffs(mrem) - 1;
+                                mrem &= mrem - 1;
+                                const int32_t rj = __shfl_sync(0xffffffffu, r, j);
+                                wt[q] = __shfl_sync(0xffffffffu, w, j);
+                                src[q] = p.expert_out + static_cast<int64_t>(rj) * row_bytes + col_bytes;
+                            } else if (has_sh && ii == n_exp) {
+                                src[q] = p.shared + t * row_bytes + col_bytes;
+                            } else {
+                                src[q] = p.residual + t * row_bytes + col_bytes;
+                            }
                         }
                     }
-                }
-                const bool last = (i + ns >= n);
-                bool good = true;
-                if (lane == 0) {
-                    good = mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, kWaitLimitNs);
-                    if (good) {
-                        StageMeta &m = meta[stage];
-                        m.t = static_cast<int32_t>(t);
-                        m.n = ns;
-                        m.flags = (last ? F_LAST : 0) | ((last && has_res && ns > 0) ? F_RESID : 0);
+                    const bool last = (i + ns >= n);
+                    bool good = true;
+                    if (lane == 0) {
+                        good = mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, kWaitLimitNs);
+                        if (good) {
+                            StageMeta &m = meta[stage];
+                            m.t = static_cast<int32_t>(t);
+                            m.n = ns;
+                            m.flags = (last ? F_LAST : 0) | ((last && has_res && ns > 0) ? F_RESID : 0);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            m.w[q] = q < RMAX ? wt[q < RMAX ? q : 0] : 1.f;
-                        const uint32_t full = full0 + 8u * stage;
-                        if (ns > 0) {
-                            mbar_arrive_expect_tx(full, static_cast<uint32_t>(ns) * row_bytes);
-                            const uint32_t dst = ring + static_cast<uint32_t>(stage) * L.slot_stride;
+                            for (int q = 0; q < 4; ++q)
+                                m.w[q] = q < RMAX ? wt[q < RMAX ? q : 0] : 1.f;
+                            const uint32_t full = full0 + 8u * stage;
+                            if (ns > 0) {
+                                mbar_arrive_expect_tx(full, static_cast<uint32_t>(ns) * copy_bytes);
+                                const uint32_t dst = ring + static_cast<uint32_t>(stage) * L.slot_stride;
 #pragma unroll
-                            for (int q = 0; q < RMAX; ++q)
-                                if (q < ns)
-                                    bulk_g2s(dst + static_cast<uint32_t>(q) * L.row_stride, src[q], row_bytes, full);
-                        } else {
-                            mbar_arrive(full);
+                                for (int q = 0; q < RMAX; ++q)
+                                    if (q < ns)
+                                        bulk_g2s(dst + static_cast<uint32_t>(q) * L.row_stride, src[q], copy_bytes,
+                                                 full);
+                            } else {
+                                mbar_arrive(full);
+                            }
                         }
                     }
-                }
-                good = __shfl_sync(0xffffffffu, good, 0);
-                if (!good) {
-                    ok = false;
-                    break;
-                }
-                ++issued;
-                if (++stage == S) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-                i += ns;
-            } while (i < n);
-        }
-        if (!ok && lane == 0) {
-            // a slot never freed up: record it, then let every copy this warp
-            // started land before the CTA's shared memory goes away
-            report(p.status, MOE_ERR_DEVICE_TIMEOUT);
-            const int64_t nn = issued < S ? issued : S;
-            for (int64_t s = 0; s < nn; ++s) {
-                const int64_t times = (issued - 1 - s) / S + 1;
-                mbar_wait_bounded(full0 + 8u * static_cast<uint32_t>(s), static_cast<uint32_t>((times - 1) & 1),
-                                  kWaitLimitNs);
+                    good = __shfl_sync(0xffffffffu, good, 0);
+                    if (!good) {
+                        ok = false;
+                        break;
+                    }
+                    ++issued;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    i += ns;
+                } while (i < n);
             }
-        }
-        return;
-    }
-
-    // ----------------------------------------------------------- consumers
-    const int tid = threadIdx.x;
-    // pad rows of a swizzled scale matrix are written as zero
-    if (QUANT != MOE_QUANT_NONE && p.sf_layout == MOE_SF_SWIZZLED_128x4 && p.sf_rows_pad > p.T) {
-        const int64_t nz = (p.sf_rows_pad - p.T) * p.sf_cols_pad;
-        for (int64_t i = static_cast<int64_t>(blockIdx.x) * NC + tid; i < nz;
-             i += static_cast<int64_t>(gridDim.x) * NC)
-            p.scales_out[sf_offset(p.T + i / p.sf_cols_pad, i % p.sf_cols_pad, p)] = 0;
-    }
-    const bool do_norm = p.gamma != nullptr;
-    const int max_slots = k + 3;  // a token never needs more slots than rows + 1
-
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t tok = 0;
-    for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, ++tok) {
-        float acc[VPT][8];
-#pragma unroll
-        for (int s = 0; s < VPT; ++s)
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                acc[s][i] = 0.f;
-        bool combined_done = false;
-        for (int it = 0; it < max_slots; ++it) {
-            if (!mbar_wait_bounded(full0 + 8u * stage, phase, kWaitLimitNs)) {
+            if (!ok && lane == 0) {
+                // a slot never freed up: record it, then let every copy this
+                // warp started land before the CTA's shared memory goes away
                 report(p.status, MOE_ERR_DEVICE_TIMEOUT);
-                return;
-            }
-            const StageMeta m = meta[stage];
-            const uint8_t *slot = smem + static_cast<uint32_t>(stage) * L.slot_stride;
-            uint4 q[RMAX][VPT];
-#pragma unroll
-            for (int rr = 0; rr < RMAX; ++rr)
-#pragma unroll
-                for (int s = 0; s < VPT; ++s) {
-                    const int v = s * NC + tid;
-                    q[rr][s] = make_uint4(0, 0, 0, 0);
-                    if (rr < m.n && v < nvec)
-                        q[rr][s] = *reinterpret_cast<const uint4 *>(slot + rr * L.row_stride + 16 * v);
+                const int64_t nn = issued < S ? issued : S;
+                for (int64_t s = 0; s < nn; ++s) {
+                    const int64_t times = (issued - 1 - s) / S + 1;
+                    mbar_wait_bounded(full0 + 8u * static_cast<uint32_t>(s), static_cast<uint32_t>((times - 1) & 1),
+                                      kWaitLimitNs);
                 }
+            }
+        }();
+    } else {
+        // ----------------------------------------------------------- consumers
+        [&]() {
+            const int tid = threadIdx.x;
+            // pad rows of a swizzled scale matrix are written as zero
+            if (QUANT != MOE_QUANT_NONE && p.sf_layout == MOE_SF_SWIZZLED_128x4 && p.sf_rows_pad > p.T) {
+                const int64_t nz = (p.sf_rows_pad - p.T) * p.sf_cols_pad;
+                for (int64_t i = static_cast<int64_t>(blockIdx.x) * NC + tid; i < nz;
+                     i += static_cast<int64_t>(gridDim.x) * NC)
+                    p.scales_out[sf_offset(p.T + i / p.sf_cols_pad, i % p.sf_cols_pad, p)] = 0;
+            }
+            const bool do_norm = p.gamma != nullptr;
+            const int max_slots = k + 3;  // a token never needs more slots than rows + 1
+
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t tok = 0;
+            for (int64_t t = unit0; t < p.T; t += nunits(), ++tok) {
+                float acc[VPT][8];
 #pragma unroll
-            for (int rr = 0; rr < RMAX; ++rr) {
-                if (rr >= m.n)
-                    break;
-                if ((m.flags & F_RESID) && rr == m.n - 1 && p.combined_out) {
+                for (int s = 0; s < VPT; ++s)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        acc[s][i] = 0.f;
+                bool combined_done = false;
+                for (int it = 0; it < max_slots; ++it) {
+                    // a give-up is taken by the whole warp, so that no lane is
+                    // left behind in the warp-wide shuffles below
+                    if (__any_sync(0xffffffffu, !mbar_wait_bounded(full0 + 8u * stage, phase, kWaitLimitNs))) {
+                        report(p.status, MOE_ERR_DEVICE_TIMEOUT);
+                        return;
+                    }
+                    const StageMeta m = meta[stage];
+                    const uint8_t *slot = smem + static_cast<uint32_t>(stage) * L.slot_stride;
+                    uint4 q[RMAX][VPT];
+#pragma unroll
+                    for (int rr = 0; rr < RMAX; ++rr)
+#pragma unroll
+                        for (int s = 0; s < VPT; ++s) {
+                            const int v = s * NC + tid;
+                            q[rr][s] = make_uint4(0, 0, 0, 0);
+                            if (rr < m.n && v < nvec)
+                                q[rr][s] = *reinterpret_cast<const uint4 *>(slot + rr * L.row_stride + 16 * v);
+                        }
+#pragma unroll
+                    for (int rr = 0; rr < RMAX; ++rr) {
+                        if (rr >= m.n)
+                            break;
+                        if ((m.flags & F_RESID) && rr == m.n - 1 && p.combined_out) {
+#pragma unroll
+                            for (int s = 0; s < VPT; ++s) {
+                                const int v = s * NC + tid;
+                                if (v < nvec)
+                                    store16x8<IO>(p.combined_out, t * H + col0 + 8 * v, acc[s]);
+                            }
+                            combined_done = true;
+                        }
+                        const float wr = m.w[rr];
+#pragma unroll
+                        for (int s = 0; s < VPT; ++s) {
+                            const int v = s * NC + tid;
+                            if (v < nvec) {
+                                const uint32_t qw[4] = {q[rr][s].x, q[rr][s].y, q[rr][s].z, q[rr][s].w};
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    float lo, hi;
+                                    unpack16x2<IO>(qw[i], lo, hi);
+                                    fma2(acc[s][2 * i], acc[s][2 * i + 1], lo, hi, wr);
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(empty0 + 8u * stage);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    if (m.flags & F_LAST)
+                        break;
+                }
+
+                // -------------------------------------------------- epilogue
+                const int64_t row0 = t * H + col0;  // element offset of this CTA's slice of row t
+                if (p.combined_out && !combined_done) {
 #pragma unroll
                     for (int s = 0; s < VPT; ++s) {
                         const int v = s * NC + tid;
                         if (v < nvec)
-                            store16x8<IO>(p.combined_out, t * H + 8 * v, acc[s]);
+                            store16x8<IO>(p.combined_out, row0 + 8 * v, acc[s]);
                     }
-                    combined_done = true;
                 }
-                const float wr = m.w[rr];
+                if (p.residual_out) {
 #pragma unroll
-                for (int s = 0; s < VPT; ++s) {
-                    const int v = s * NC + tid;
-                    if (v < nvec) {
-                        const uint32_t qw[4] = {q[rr][s].x, q[rr][s].y, q[rr][s].z, q[rr][s].w};
+                    for (int s = 0; s < VPT; ++s) {
+                        const int v = s * NC + tid;
+                        if (v < nvec)
+                            store16x8<IO>(p.residual_out, row0 + 8 * v, acc[s]);
+                    }
+                }
+                if (do_norm) {
+                    // gamma is re-read per token; it stays in L1 / L2
+                    uint4 gq[VPT];
+#pragma unroll
+                    for (int s = 0; s < VPT; ++s) {
+                        const int v = s * NC + tid;
+                        gq[s] = (v < nvec) ? __ldg(reinterpret_cast<const uint4 *>(p.gamma + col0) + v)
+                                           : make_uint4(0, 0, 0, 0);
+                    }
+                    float ss = 0.f;
+#pragma unroll
+                    for (int s = 0; s < VPT; ++s)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            ss = fmaf(acc[s][i], acc[s][i], ss);  // vectors past the slice hold 0
+#pragma unroll
+                    for (int d = 16; d > 0; d >>= 1)
+                        ss += __shfl_xor_sync(0xffffffffu, ss, d);
+                    float total = 0.f;
+                    if constexpr (SPLIT) {
+                        // every warp of every CTA of the cluster sends its partial
+                        // to slot [rank][warp] of every CTA (lane r to CTA r) and
+                        // arrives there; each CTA then adds all csize * ncw of
+                        // them in the same order, so the whole token sees one
+                        // norm.  Buffers and barriers alternate with the token's
+                        // parity: a CTA can run at most one token ahead of a peer
+                        // that has not yet read its partials.
+                        const uint32_t par = tok & 1u;
+                        float *part = red + par * csize * static_cast<uint32_t>(ncw);
+                        __syncwarp();
+                        if (static_cast<uint32_t>(lane) < csize) {
+                            const uint32_t mine = smem_u32(part + crank * ncw + warp);
+                            st_cluster_f32(cluster_map(mine, lane), ss);
+                            mbar_arrive_cluster(cluster_map(xbar0 + 8u * par, lane));
+                        }
+                        if (__any_sync(0xffffffffu,
+                                       !mbar_wait_cluster_bounded(xbar0 + 8u * par, (tok >> 1) & 1u, kWaitLimitNs))) {
+                            report(p.status, MOE_ERR_DEVICE_TIMEOUT);
+                            return;
+                        }
+                        const int np = static_cast<int>(csize) * ncw;
+                        for (int w = 0; w < np; ++w)
+                            total += part[w];
+                    } else {
+                        float *part = red + (tok & 1u) * ncw;
+                        if (lane == 0) {
+                            part[warp] = ss;
+                            mbar_arrive(redbar);
+                        }
+                        if (__any_sync(0xffffffffu, !mbar_wait_bounded(redbar, tok & 1u, kWaitLimitNs))) {
+                            report(p.status, MOE_ERR_DEVICE_TIMEOUT);
+                            return;
+                        }
+                        for (int w = 0; w < ncw; ++w)
+                            total += part[w];
+                    }
+                    const float rinv = 1.0f / sqrtf(total / static_cast<float>(H) + p.eps);
+#pragma unroll
+                    for (int s = 0; s < VPT; ++s) {
+                        const uint32_t gv[4] = {gq[s].x, gq[s].y, gq[s].z, gq[s].w};
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             float lo, hi;
-                            unpack16x2<IO>(qw[i], lo, hi);
-                            fma2(acc[s][2 * i], acc[s][2 * i + 1], lo, hi, wr);
+                            unpack16x2<IO>(gv[i], lo, hi);
+                            acc[s][2 * i] = acc[s][2 * i] * rinv * (lo + p.wb);
+                            acc[s][2 * i + 1] = acc[s][2 * i + 1] * rinv * (hi + p.wb);
+                        }
+                    }
+                    if (p.norm_out) {
+#pragma unroll
+                        for (int s = 0; s < VPT; ++s) {
+                            const int v = s * NC + tid;
+                            if (v < nvec)
+                                store16x8<IO>(p.norm_out, row0 + 8 * v, acc[s]);
+                        }
+                    }
+                }
+
+                if constexpr (QUANT == MOE_QUANT_MXFP8) {
+#pragma unroll
+                    for (int s = 0; s < VPT; ++s) {
+                        const int v = s * NC + tid;
+                        const bool vv = v < nvec;
+                        float amax = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            amax = fmaxf(amax, fabsf(acc[s][i]));
+                        amax = vv ? amax : 0.f;
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                        const int32_t byte = ue8m0_byte(amax);
+                        const float scale = __uint_as_float(static_cast<uint32_t>(254 - byte) << 23);  // 2^-e
+                        if (vv) {
+                            uint2 qv;
+                            qv.x = cvt_e4m3x4(acc[s][0] * scale, acc[s][1] * scale, acc[s][2] * scale,
+                                              acc[s][3] * scale);
+                            qv.y = cvt_e4m3x4(acc[s][4] * scale, acc[s][5] * scale, acc[s][6] * scale,
+                                              acc[s][7] * scale);
+                            *reinterpret_cast<uint2 *>(p.quant_out + row0 + 8 * v) = qv;
+                            if ((lane & 3) == 0) {
+                                const int64_t c = (vec0 + v) >> 2;
+                                p.scales_out[sf_offset(t, c, p)] = static_cast<uint8_t>(byte);
+                                if (c == p.sf_cols - 1)
+                                    for (int64_t cp = p.sf_cols; cp < p.sf_cols_pad; ++cp)
+                                        p.scales_out[sf_offset(t, cp, p)] = 0;
+                            }
+                        }
+                    }
+                } else if constexpr (QUANT == MOE_QUANT_MXFP4) {
+#pragma unroll
+                    for (int s = 0; s < VPT; ++s) {
+                        const int v = s * NC + tid;
+                        const bool vv = v < nvec;
+                        float amax = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            amax = fmaxf(amax, fabsf(acc[s][i]));
+                        amax = vv ? amax : 0.f;
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                        const int32_t byte = ue8m0_fp4_byte(amax);
+                        const float scale = __uint_as_float(static_cast<uint32_t>(254 - byte) << 23);  // 2^-e
+                        if (vv) {
+                            float qv[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                qv[i] = acc[s][i] * scale;
+                            *reinterpret_cast<uint32_t *>(p.quant_out + (row0 >> 1) + 4 * v) = cvt_e2m1x8(qv);
+                            if ((lane & 3) == 0) {
+                                const int64_t c = (vec0 + v) >> 2;
+                                p.scales_out[sf_offset(t, c, p)] = static_cast<uint8_t>(byte);
+                                if (c == p.sf_cols - 1)
+                                    for (int64_t cp = p.sf_cols; cp < p.sf_cols_pad; ++cp)
+                                        p.scales_out[sf_offset(t, cp, p)] = 0;
+                            }
+                        }
+                    }
+                } else if constexpr (QUANT == MOE_QUANT_NVFP4) {
+#pragma unroll
+                    for (int s = 0; s < VPT; ++s) {
+                        const int v = s * NC + tid;
+                        const bool vv = v < nvec;
+                        float g[8];
+                        float amax = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            g[i] = acc[s][i] * p.gscale;
+                            amax = fmaxf(amax, fabsf(g[i]));
+                        }
+                        amax = vv ? amax : 0.f;
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                        const uint32_t sc = cvt_e4m3x2(__fdiv_rn(amax, 6.0f), 0.f) & 0xFFu;
+                        const float sf = e4m3_code_value(sc);
+                        if (vv) {
+                            uint32_t packed = 0;
+                            if (sf != 0.f) {
+                                // elements are scaled by the block scale's correctly
+                                // rounded fp32 reciprocal
+                                const float rs = __frcp_rn(sf);
+                                float qv[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    qv[i] = g[i] * rs;
+                                packed = cvt_e2m1x8(qv);
+                            }
+                            *reinterpret_cast<uint32_t *>(p.quant_out + (row0 >> 1) + 4 * v) = packed;
+                            if ((lane & 1) == 0) {
+                                const int64_t c = (vec0 + v) >> 1;
+                                p.scales_out[sf_offset(t, c, p)] = static_cast<uint8_t>(sc);
+                                if (c == p.sf_cols - 1)
+                                    for (int64_t cp = p.sf_cols; cp < p.sf_cols_pad; ++cp)
+                                        p.scales_out[sf_offset(t, cp, p)] = 0;
+                            }
                         }
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(empty0 + 8u * stage);
-            if (++stage == S) {
-                stage = 0;
-                phase ^= 1u;
-            }
-            if (m.flags & F_LAST)
-                break;
-        }
-
-        // ------------------------------------------------------ epilogue
-        const int64_t row0 = t * H;
-        if (p.combined_out && !combined_done) {
-#pragma unroll
-            for (int s = 0; s < VPT; ++s) {
-                const int v = s * NC + tid;
-                if (v < nvec)
-                    store16x8<IO>(p.combined_out, row0 + 8 * v, acc[s]);
-            }
-        }
-        if (p.residual_out) {
-#pragma unroll
-            for (int s = 0; s < VPT; ++s) {
-                const int v = s * NC + tid;
-                if (v < nvec)
-                    store16x8<IO>(p.residual_out, row0 + 8 * v, acc[s]);
-            }
-        }
-        if (do_norm) {
-            // gamma is re-read per token; it stays in L1 / L2
-            uint4 gq[VPT];
-#pragma unroll
-            for (int s = 0; s < VPT; ++s) {
-                const int v = s * NC + tid;
-                gq[s] = (v < nvec) ? __ldg(reinterpret_cast<const uint4 *>(p.gamma) + v) : make_uint4(0, 0, 0, 0);
-            }
-            float ss = 0.f;
-#pragma unroll
-            for (int s = 0; s < VPT; ++s)
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    ss = fmaf(acc[s][i], acc[s][i], ss);  // vectors past H hold 0
-#pragma unroll
-            for (int d = 16; d > 0; d >>= 1)
-                ss += __shfl_xor_sync(0xffffffffu, ss, d);
-            float *part = red + (tok & 1u) * ncw;
-            if (lane == 0) {
-                part[warp] = ss;
-                mbar_arrive(redbar);
-            }
-            if (!mbar_wait_bounded(redbar, tok & 1u, kWaitLimitNs)) {
-                report(p.status, MOE_ERR_DEVICE_TIMEOUT);
-                return;
-            }
-            float total = 0.f;
-            for (int w = 0; w < ncw; ++w)
-                total += part[w];
-            const float rinv = 1.0f / sqrtf(total / static_cast<float>(H) + p.eps);
-#pragma unroll
-            for (int s = 0; s < VPT; ++s) {
-                const uint32_t gv[4] = {gq[s].x, gq[s].y, gq[s].z, gq[s].w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float lo, hi;
-                    unpack16x2<IO>(gv[i], lo, hi);
-                    acc[s][2 * i] = acc[s][2 * i] * rinv * (lo + p.wb);
-                    acc[s][2 * i + 1] = acc[s][2 * i + 1] * rinv * (hi + p.wb);
-                }
-            }
-            if (p.norm_out) {
-#pragma unroll
-                for (int s = 0; s < VPT; ++s) {
-                    const int v = s * NC + tid;
-                    if (v < nvec)
-                        store16x8<IO>(p.norm_out, row0 + 8 * v, acc[s]);
-                }
-            }
-        }
-
-        if constexpr (QUANT == MOE_QUANT_MXFP8) {
-#pragma unroll
-            for (int s = 0; s < VPT; ++s) {
-                const int v = s * NC + tid;
-                const bool vv = v < nvec;
-                float amax = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    amax = fmaxf(amax, fabsf(acc[s][i]));
-                amax = vv ? amax : 0.f;
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-                const int32_t byte = ue8m0_byte(amax);
-                const float scale = __uint_as_float(static_cast<uint32_t>(254 - byte) << 23);  // 2^-e
-                if (vv) {
-                    uint2 qv;
-                    qv.x = cvt_e4m3x4(acc[s][0] * scale, acc[s][1] * scale, acc[s][2] * scale, acc[s][3] * scale);
-                    qv.y = cvt_e4m3x4(acc[s][4] * scale, acc[s][5] * scale, acc[s][6] * scale, acc[s][7] * scale);
-                    *reinterpret_cast<uint2 *>(p.quant_out + row0 + 8 * v) = qv;
-                    if ((lane & 3) == 0) {
-                        const int64_t c = v >> 2;
-                        p.scales_out[sf_offset(t, c, p)] = static_cast<uint8_t>(byte);
-                        if (c == p.sf_cols - 1)
-                            for (int64_t cp = p.sf_cols; cp < p.sf_cols_pad; ++cp)
-                                p.scales_out[sf_offset(t, cp, p)] = 0;
-                    }
-                }
-            }
-        } else if constexpr (QUANT == MOE_QUANT_MXFP4) {
-#pragma unroll
-            for (int s = 0; s < VPT; ++s) {
-                const int v = s * NC + tid;
-                const bool vv = v < nvec;
-                float amax = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    amax = fmaxf(amax, fabsf(acc[s][i]));
-                amax = vv ? amax : 0.f;
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-                const int32_t byte = ue8m0_fp4_byte(amax);
-                const float scale = __uint_as_float(static_cast<uint32_t>(254 - byte) << 23);  // 2^-e
-                if (vv) {
-                    float qv[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        qv[i] = acc[s][i] * scale;
-                    *reinterpret_cast<uint32_t *>(p.quant_out + (row0 >> 1) + 4 * v) = cvt_e2m1x8(qv);
-                    if ((lane & 3) == 0) {
-                        const int64_t c = v >> 2;
-                        p.scales_out[sf_offset(t, c, p)] = static_cast<uint8_t>(byte);
-                        if (c == p.sf_cols - 1)
-                            for (int64_t cp = p.sf_cols; cp < p.sf_cols_pad; ++cp)
-                                p.scales_out[sf_offset(t, cp, p)] = 0;
-                    }
-                }
-            }
-        } else if constexpr (QUANT == MOE_QUANT_NVFP4) {
-#pragma unroll
-            for (int s = 0; s < VPT; ++s) {
-                const int v = s * NC + tid;
-                const bool vv = v < nvec;
-                float g[8];
-                float amax = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    g[i] = acc[s][i] * p.gscale;
-                    amax = fmaxf(amax, fabsf(g[i]));
-                }
-                amax = vv ? amax : 0.f;
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                const uint32_t sc = cvt_e4m3x2(__fdiv_rn(amax, 6.0f), 0.f) & 0xFFu;
-                const float sf = e4m3_code_value(sc);
-                if (vv) {
-                    uint32_t packed = 0;
-                    if (sf != 0.f) {
-                        // elements are scaled by the block scale's correctly
-                        // rounded fp32 reciprocal
-                        const float rs = __frcp_rn(sf);
-                        float qv[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            qv[i] = g[i] * rs;
-                        packed = cvt_e2m1x8(qv);
-                    }
-                    *reinterpret_cast<uint32_t *>(p.quant_out + (row0 >> 1) + 4 * v) = packed;
-                    if ((lane & 1) == 0) {
-                        const int64_t c = v >> 1;
-                        p.scales_out[sf_offset(t, c, p)] = static_cast<uint8_t>(sc);
-                        if (c == p.sf_cols - 1)
-                            for (int64_t cp = p.sf_cols; cp < p.sf_cols_pad; ++cp)
-                                p.scales_out[sf_offset(t, cp, p)] = 0;
-                    }
-                }
-            }
-        }
+        }();
     }
+    // with SPLIT, no CTA leaves while a peer may still write into its shared
+    // memory or arrive on its barriers (every wait above is bounded, so every
+    // thread gets here)
+    if constexpr (SPLIT)
+        cluster_arrive_wait();
 }
 
 // ------------------------------------------------------------------- host
 
 // Process-wide plan overrides set by moe_tuning_set (0 = automatic).
 struct Tuning {
-    int vpt = 0, rows = 0, ring_kib = 0, ctas_per_sm = 0;
+    int vpt = 0, rows = 0, ring_kib = 0, ctas_per_sm = 0, split = 0;
 };
 extern Tuning g_tuning;
 
 struct Plan {
     int vpt, ncw, rows, stages, ctas_per_sm;
+    int split, hl;  // CTAs per token (cluster size) and the columns each handles
     SmemLayout smem;
 };
 
-// Vectors per consumer thread: the smallest of 1, 2, 4, 8 that needs at most
-// 16 consumer warps.  Rows per ring slot: as many as the registers allow (4
-// for VPT <= 2).  Measured on GB300: at H = 7168, 14 warps x 2 vectors with 4
-// rows per slot reach 93 % of HBM copy bandwidth, against 73 % for 7 warps x 4
-// (latency-bound) and 80 % for 28 warps x 1 (per-row overhead); at H = 4096,
-// 16 warps x 1 beat 8 x 2.  Ring: about kDefaultRingBytes of rows, at least 2
-// slots, within the shared-memory budget.
-inline Plan make_plan(int32_t H)
+constexpr int kMaxSplit = 16;
+constexpr int kMaxSplitCols = 4096;  // a slice fits 16 consumer warps at one vector each
+
+// Whether `c` CTAs can share a row of H: equal slices that hold whole quant
+// blocks and at most kMaxSplitCols columns.
+inline bool split_ok(int32_t H, int32_t quant, int c)
+{
+    const int blk = quant == MOE_QUANT_NVFP4 ? 16 : (quant == MOE_QUANT_NONE ? 8 : 32);
+    return c >= 2 && c <= kMaxSplit && H % (c * blk) == 0 && H / c <= kMaxSplitCols;
+}
+
+constexpr int kMinAutoSplitCols = 256;  // one vector per lane of one full warp
+
+// CTAs per token.  One CTA per token streams a row set through one SM; with
+// fewer tokens than SMs most of the GPU would idle, so a token is spread over
+// the smallest cluster of 2, 4, 8 or 16 CTAs that gives every SM work (or the
+// largest allowed), keeping slices of at least kMinAutoSplitCols columns.
+// moe_tuning_set may force 1 or a cluster size.
+inline int choose_split(int32_t H, int64_t T, int32_t quant, int forced)
+{
+    if (forced == 1)
+        return 1;
+    if (forced >= 2)
+        return split_ok(H, quant, forced) ? forced : 1;
+    const int sms = sm_count();
+    if (sms <= 0 || T >= sms)
+        return 1;
+    int best = 1;
+    for (int c = 2; c <= kMaxSplit && H / c >= kMinAutoSplitCols; c *= 2) {
+        if (!split_ok(H, quant, c))
+            continue;
+        best = c;
+        if (T * c >= sms)
+            break;
+    }
+    return best;
+}
+
+// Whole rows (split 1): vectors per consumer thread, the smallest of 1, 2,
+// 4, 8 that needs at most 16 consumer warps.  Rows per ring slot: as many as
+// the registers allow (4 for VPT <= 2).  Measured on GB300: at H = 7168, 14
+// warps x 2 vectors with 4 rows per slot reach 93 % of HBM copy bandwidth,
+// against 73 % for 7 warps x 4 (latency-bound) and 80 % for 28 warps x 1
+// (per-row overhead); at H = 4096, 16 warps x 1 beat 8 x 2.  Ring: about
+// kDefaultRingBytes of rows, at least 2 slots, within the shared-memory
+// budget.
+// Split rows: one vector per thread over the H / split columns, and a ring
+// that holds a whole token (k + 2 rows), so that the producer never waits
+// inside a token and several CTAs fit on one SM.
+inline Plan make_plan(int32_t H, int64_t T, int32_t k, int32_t quant, int split_request)
 {
     const Tuning tu = g_tuning;
     Plan pl{};
-    const int nvec = H / 8;
+    pl.split = choose_split(H, T, quant, split_request);
+    pl.hl = H / pl.split;
+    const int nvec = pl.hl / 8;
     auto covers = [&](int v) { return (nvec + 32 * v - 1) / (32 * v) <= max_consumer_warps_rt(v); };
     pl.vpt = 8;
-    if (tu.vpt && covers(tu.vpt)) {
+    if (pl.split > 1) {
+        pl.vpt = 1;
+    } else if (tu.vpt && covers(tu.vpt)) {
         pl.vpt = tu.vpt;
     } else {
         for (int v : {1, 2, 4, 8}) {
@@ -594,23 +710,29 @@ inline Plan make_plan(int32_t H)
     pl.ctas_per_sm = tu.ctas_per_sm ? tu.ctas_per_sm : 1;
     // one CTA keeps kSmemBudget; several share the SM's 228 KB (1 KB reserved each)
     const size_t budget = pl.ctas_per_sm == 1 ? kSmemBudget : (224 * 1024) / pl.ctas_per_sm - 2048;
-    const SmemLayout one = smem_layout(H, 1, pl.rows, pl.ncw);
+    const SmemLayout one = smem_layout(pl.hl, 1, pl.rows, pl.ncw, pl.split);
     const size_t per_slot = one.slot_stride + 16 + sizeof(StageMeta);
     const size_t fixed = one.total - per_slot;
-    const size_t ring = tu.ring_kib ? static_cast<size_t>(tu.ring_kib) * 1024 : kDefaultRingBytes;
-    int s = static_cast<int>((ring + one.slot_stride / 2) / one.slot_stride);
+    int s;
+    if (tu.ring_kib) {
+        s = static_cast<int>((static_cast<size_t>(tu.ring_kib) * 1024 + one.slot_stride / 2) / one.slot_stride);
+    } else if (pl.split > 1) {
+        s = (k + 2 + pl.rows - 1) / pl.rows;
+    } else {
+        s = static_cast<int>((kDefaultRingBytes + one.slot_stride / 2) / one.slot_stride);
+    }
     const int fit = budget > fixed ? static_cast<int>((budget - fixed) / per_slot) : 0;
     s = s > fit ? fit : s;
     s = s > kMaxStages ? kMaxStages : s;
     pl.stages = s < 2 ? 2 : s;
-    pl.smem = smem_layout(H, pl.stages, pl.rows, pl.ncw);
+    pl.smem = smem_layout(pl.hl, pl.stages, pl.rows, pl.ncw, pl.split);
     return pl;
 }
 
-template <int VPT, int QUANT, int IO>
+template <int VPT, int QUANT, int IO, bool SPLIT>
 moe_status launch_t(const Params &p, const Plan &pl, cudaStream_t stream)
 {
-    auto kern = combine_kernel<VPT, QUANT, IO>;
+    auto kern = combine_kernel<VPT, QUANT, IO, SPLIT>;
     static int configured_for[64] = {0};  // per device: dynamic smem already allowed
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
@@ -621,25 +743,69 @@ moe_status launch_t(const Params &p, const Plan &pl, cudaStream_t stream)
     if (dev < 0 || dev >= 64 || configured_for[dev] < need) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, need) != cudaSuccess)
             return MOE_ERR_CUDA;
+        if (SPLIT && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+            return MOE_ERR_CUDA;
         if (dev >= 0 && dev < 64)
             configured_for[dev] = need;
     }
-    const int64_t ctas = static_cast<int64_t>(sm_count()) * pl.ctas_per_sm;
-    if (ctas <= 0)
-        return MOE_ERR_CUDA;
-    const int grid = static_cast<int>(p.T < ctas ? p.T : ctas);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(pl.split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
     // programmatic dependent launch: the kernel may be scheduled while the
     // previous kernel on the stream finishes; it waits for it before reading
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(grid);
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3((pl.ncw + 1) * 32);
     cfg.dynamicSmemBytes = pl.smem.total;
     cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    if (SPLIT) {
+        // a cluster that no GPC can hold is reported as unsupported (the
+        // caller then falls back to whole rows); the answer is kept per
+        // device, cluster size and shared-memory size
+        static int fits_split[64][5], fits_smem[64][5];
+        int li = 0;
+        while ((2 << li) < pl.split)
+            ++li;
+        if (dev < 0 || dev >= 64 || fits_smem[dev][li] != need) {
+            cfg.gridDim = dim3(static_cast<unsigned>(pl.split));
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+            if (dev < 0 || dev >= 64) {
+                if (n < 1)
+                    return MOE_ERR_UNSUPPORTED;
+            } else {
+                fits_split[dev][li] = n;
+                fits_smem[dev][li] = need;
+            }
+        }
+        if (dev >= 0 && dev < 64 && fits_split[dev][li] < 1)
+            return MOE_ERR_UNSUPPORTED;
+    }
+    const int64_t sms = sm_count();
+    if (sms <= 0)
+        return MOE_ERR_CUDA;
+    int64_t grid;
+    if (SPLIT) {
+        // one cluster per token, up to four clusters' worth of CTAs per SM;
+        // clusters never wait on one another, so any that do not fit at
+        // once simply start later
+        const int64_t most = (4 * sms) / pl.split;
+        grid = (p.T < most ? p.T : most) * pl.split;
+    } else {
+        const int64_t ctas = sms * pl.ctas_per_sm;
+        grid = p.T < ctas ? p.T : ctas;
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.attrs = SPLIT ? attr : attr + 1;
+    cfg.numAttrs = SPLIT ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) {
         cudaGetLastError();
         return MOE_ERR_CUDA;
@@ -650,11 +816,13 @@ moe_status launch_t(const Params &p, const Plan &pl, cudaStream_t stream)
 template <int QUANT, int IO>
 moe_status launch_q(const Params &p, const Plan &pl, cudaStream_t stream)
 {
+    if (pl.split > 1)
+        return launch_t<1, QUANT, IO, true>(p, pl, stream);
     switch (pl.vpt) {
-    case 1: return launch_t<1, QUANT, IO>(p, pl, stream);
-    case 2: return launch_t<2, QUANT, IO>(p, pl, stream);
-    case 4: return launch_t<4, QUANT, IO>(p, pl, stream);
-    default: return launch_t<8, QUANT, IO>(p, pl, stream);
+    case 1: return launch_t<1, QUANT, IO, false>(p, pl, stream);
+    case 2: return launch_t<2, QUANT, IO, false>(p, pl, stream);
+    case 4: return launch_t<4, QUANT, IO, false>(p, pl, stream);
+    default: return launch_t<8, QUANT, IO, false>(p, pl, stream);
     }
 }
 

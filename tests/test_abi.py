@@ -93,14 +93,16 @@ def test_combine_validation(L, kw, want):
 
 
 def test_tuning_validation(L):
-    assert L.moe_tuning_set(3, 0, 0, 0, 0) == 1
-    assert L.moe_tuning_set(0, 5, 0, 0, 0) == 1
-    assert L.moe_tuning_set(0, 0, 300, 0, 0) == 1
-    assert L.moe_tuning_set(0, 0, 0, 9, 0) == 1
-    assert L.moe_tuning_set(0, 0, 0, 0, 17) == 1
-    assert L.moe_tuning_set(0, 0, 0, 0, -2) == 1
-    assert L.moe_tuning_set(2, 2, 144, 1, -1) == 0
-    assert L.moe_tuning_set(0, 0, 0, 0, 0) == 0
+    assert L.moe_tuning_set(3, 0, 0, 0, 0, 0) == 1
+    assert L.moe_tuning_set(0, 5, 0, 0, 0, 0) == 1
+    assert L.moe_tuning_set(0, 0, 300, 0, 0, 0) == 1
+    assert L.moe_tuning_set(0, 0, 0, 9, 0, 0) == 1
+    assert L.moe_tuning_set(0, 0, 0, 0, 17, 0) == 1
+    assert L.moe_tuning_set(0, 0, 0, 0, -2, 0) == 1
+    for bad in (-1, 3, 6, 32):
+        assert L.moe_tuning_set(0, 0, 0, 0, 0, bad) == 1
+    assert L.moe_tuning_set(2, 2, 144, 1, -1, 8) == 0
+    assert L.moe_tuning_set(0, 0, 0, 0, 0, 0) == 0
 
 
 def test_combine_null_args(L):

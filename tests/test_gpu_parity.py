@@ -307,3 +307,80 @@ def test_dtype_and_mxfp4_parity(kw):
     got = gpu_combine(wl, inp, d_rm, global_scale=g, canary=True)
     assert got["status"] == 0
     compare(wl, inp, orm, got, global_scale=g)
+
+
+# ------------------------------------------------- split rows (decode sizes)
+
+SPLIT_CASES = [
+    # the decode workload's shape: residual + norm, bf16 outputs
+    dict(T=64, H=7168, k=8, E=256, outputs=("residual", "norm")),
+    # shared row and combined_out (stored before the residual row lands), MXFP8
+    dict(T=23, H=7168, k=8, E=256, shared_std=0.5, quant="mxfp8",
+         outputs=("combined", "residual", "quant")),
+    # Gemma form, NVFP4 with swizzled scales (pad rows and columns)
+    dict(T=5, H=4096, k=8, E=128, gamma_mean=0.0, weight_bias=1.0, quant="nvfp4", sf_layout="swizzled",
+         outputs=("residual", "norm", "quant")),
+    # fp16 inputs and outputs, fp16 router weights, MXFP4
+    dict(T=7, H=2048, k=6, E=32, io_dtype="fp16", weight_dtype="fp16", quant="mxfp4",
+         outputs=("combined", "norm", "quant")),
+    # many tokens per cluster: the reduction buffers alternate many times
+    dict(T=700, H=4096, k=8, E=128, shared_std=0.5, quant="mxfp8", outputs=("residual", "norm", "quant")),
+    # padded tokens (no expert rows) and no residual
+    dict(T=40, H=1024, k=4, E=16, pad_frac=0.5, residual=False, outputs=("combined", "norm")),
+]
+
+
+@pytest.mark.parametrize("split", [0, 1, 2, 4, 8, 16])
+@pytest.mark.parametrize("kw", SPLIT_CASES,
+                         ids=["decode", "shared_mxfp8", "gemma_nvfp4", "fp16_mxfp4", "many_tokens", "padded"])
+def test_split_rows_parity(kw, split):
+    """A token's row split by columns over a cluster of 2..16 CTAs (their
+    sums of squares exchanged through distributed shared memory) gives the
+    oracle's outputs, as whole rows do."""
+    wl = _wl(**kw)
+    inp = synth.make_inputs(wl)
+    d_rm, orm = route_and_check(inp["topk_ids"], wl.E)
+    g = nvfp4_global_scale(wl, inp, orm) if wl.quant == "nvfp4" else 1.0
+    try:
+        nqg.moe_tuning_set(combine_split=split)
+        got = gpu_combine(wl, inp, d_rm, global_scale=g, canary=True)
+    finally:
+        nqg.moe_tuning_set()
+    assert got["status"] == 0
+    compare(wl, inp, orm, got, global_scale=g)
+
+
+@pytest.mark.parametrize("split", [2, 16])
+def test_split_rows_slot_major_and_unsplittable_h(split):
+    """The split path with the slot-major layout, and a forced split on an H
+    that no cluster divides into whole MXFP8 blocks (whole rows are used)."""
+    wl = _wl(T=9, H=7168, k=8, E=1, shared_std=0.5, quant="mxfp8", outputs=("residual", "quant"))
+    inp = synth.make_slot_major_inputs(wl)
+    wl2 = _wl(T=11, H=7200, k=8, E=64, quant="mxfp8", outputs=("residual", "norm", "quant"))
+    inp2 = synth.make_inputs(wl2)
+    d_rm2, orm2 = route_and_check(inp2["topk_ids"], wl2.E)
+    try:
+        nqg.moe_tuning_set(combine_split=split)
+        got = gpu_combine(wl, inp, None, canary=True, expert_layout="slot_major")
+        got2 = gpu_combine(wl2, inp2, d_rm2, canary=True)
+    finally:
+        nqg.moe_tuning_set()
+    assert got["status"] == 0 and got2["status"] == 0
+    compare(wl, inp, None, got, expert_layout="slot_major")
+    compare(wl2, inp2, orm2, got2)
+
+
+def test_split_rows_repeatable():
+    """The cross-CTA norm adds the partials in one fixed order: two runs of
+    the split path are bit-identical."""
+    wl = _wl(T=64, H=7168, k=8, E=256, quant="mxfp8", outputs=("residual", "norm", "quant"))
+    inp = synth.make_inputs(wl)
+    d_rm, _ = route_and_check(inp["topk_ids"], wl.E)
+    try:
+        nqg.moe_tuning_set(combine_split=8)
+        a = gpu_combine(wl, inp, d_rm)
+        b = gpu_combine(wl, inp, d_rm)
+    finally:
+        nqg.moe_tuning_set()
+    for key in ("residual", "norm", "quant", "scales"):
+        assert np.array_equal(a[key], b[key])
