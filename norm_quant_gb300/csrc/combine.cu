@@ -35,12 +35,15 @@
 //   * after a token's last slot: bf16 stores, a sum of squares reduced by
 //     warp shuffles and an mbarrier-synchronised cross-warp sum, the norm,
 //     and the block quantiser (an MXFP8 block is 4 consecutive lanes, NVFP4 2);
-//   * with fewer tokens than SMs, a token is split by columns over a
+//   * on request (moe_tuning_set), a token is split by columns over a
 //     thread-block cluster of 2..16 CTAs (each copies, sums, normalises and
 //     quantises its own slice of every row); the slices' sums of squares
 //     meet through distributed shared memory: each warp stores its partial
 //     into every CTA of the cluster and arrives on that CTA's mbarrier, and
-//     each CTA adds the partials in one fixed order.
+//     each CTA adds the partials in one fixed order;
+//   * gamma's slice is copied to shared memory once per CTA, and the
+//     per-warp partial sums of squares are added by a butterfly that gives
+//     every lane the same total.
 // Every wait is bounded (kWaitLimitNs); a wait that gives up records
 // MOE_ERR_DEVICE_TIMEOUT and the CTA drains its own copies and finishes.
 #include <cstdint>
@@ -175,9 +178,9 @@ extern "C" moe_status moe_combine(const moe_combine_args *a, moe_stream_t stream
         p.hl = pl.hl;
         return a->io_dtype == MOE_IO_FP16 ? launch_io<1>(p, pl, a->quant, s) : launch_io<0>(p, pl, a->quant, s);
     };
-    const Plan pl = make_plan(a->H, a->T, a->top_k, a->quant, g_tuning.split);
+    const Plan pl = make_plan(a->H, a->T, a->top_k, a->quant, a->gamma != nullptr, g_tuning.split);
     const moe_status st = launch(pl);
     if (st == MOE_ERR_UNSUPPORTED && pl.split > 1)
-        return launch(make_plan(a->H, a->T, a->top_k, a->quant, 1));  // no room for the cluster: whole rows
+        return launch(make_plan(a->H, a->T, a->top_k, a->quant, a->gamma != nullptr, 1));  // no room for the cluster: whole rows
     return st;
 }

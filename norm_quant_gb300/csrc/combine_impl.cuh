@@ -14,15 +14,15 @@ namespace combine_detail {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kMaxStages = 32;
-constexpr size_t kSmemBudget = 200 * 1024;
+constexpr size_t kSmemBudget = 226 * 1024;
 constexpr size_t kDefaultRingBytes = 144 * 1024;
 
 // Consumer warps allowed per CTA for each VPT (vectors of 8 elements per
 // consumer thread); the CTA adds one producer warp.  Together they cover
-// H <= 7168 (VPT 1), 8192 (VPT 2, 4) and 16384 (VPT 8).
+// H <= 4096 (VPT 1), 8192 (VPT 2, 4) and 16384 (VPT 8).
 template <int VPT>
-__host__ __device__ constexpr int max_consumer_warps() { return VPT == 1 ? 28 : (VPT == 2 ? 16 : 8); }
-inline int max_consumer_warps_rt(int vpt) { return vpt == 1 ? 28 : (vpt == 2 ? 16 : 8); }
+__host__ __device__ constexpr int max_consumer_warps() { return VPT <= 2 ? 16 : 8; }
+inline int max_consumer_warps_rt(int vpt) { return vpt <= 2 ? 16 : 8; }
 // Rows a ring slot may hold, bounded by the registers the loads take.
 template <int VPT>
 __host__ __device__ constexpr int max_rows() { return VPT <= 2 ? 4 : (VPT == 4 ? 2 : 1); }
@@ -62,15 +62,16 @@ struct Params {
 };
 
 struct SmemLayout {
-    uint32_t row_stride, slot_stride, bars, meta, red, total;
+    uint32_t row_stride, slot_stride, bars, meta, red, gamma, total;
 };
 
 // Shared memory of one CTA handling Hl columns of each row: the ring, its
-// barriers (full[S], empty[S], the cross-warp reduction barrier, a pad, and
-// the two cross-CTA reduction barriers of a split token), the slots'
-// StageMeta, then two buffers of per-warp partial sums for csize CTAs.
+// barriers (full[S], empty[S], the cross-warp reduction barrier, the gamma
+// copy's barrier, and the two cross-CTA reduction barriers of a split
+// token), the slots' StageMeta, two buffers of per-warp partial sums for
+// csize CTAs, then (with a norm) the Hl gamma values.
 __host__ __device__ inline SmemLayout smem_layout(int32_t Hl, int32_t stages, int32_t rows, int32_t ncw,
-                                                  int32_t csize)
+                                                  int32_t csize, bool with_gamma)
 {
     SmemLayout L;
     L.row_stride = (static_cast<uint32_t>(Hl) * 2u + 127u) & ~127u;
@@ -78,7 +79,8 @@ __host__ __device__ inline SmemLayout smem_layout(int32_t Hl, int32_t stages, in
     L.bars = static_cast<uint32_t>(stages) * L.slot_stride;
     L.meta = L.bars + (2u * stages + 4u) * 8u;
     L.red = L.meta + static_cast<uint32_t>(stages) * static_cast<uint32_t>(sizeof(StageMeta));
-    L.total = L.red + 2u * static_cast<uint32_t>(csize) * static_cast<uint32_t>(ncw) * 4u;
+    L.gamma = (L.red + 2u * static_cast<uint32_t>(csize) * static_cast<uint32_t>(ncw) * 4u + 127u) & ~127u;
+    L.total = L.gamma + (with_gamma ? static_cast<uint32_t>(Hl) * 2u : 0u);
     return L;
 }
 
@@ -196,9 +198,10 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
     const uint32_t row_bytes = static_cast<uint32_t>(H) * 2u;  // pitch of every input row
     const uint32_t copy_bytes = static_cast<uint32_t>(Hl) * 2u;
     const uint32_t col_bytes = static_cast<uint32_t>(col0) * 2u;
-    const SmemLayout L = smem_layout(Hl, S, R, ncw, static_cast<int32_t>(csize));
+    const SmemLayout L = smem_layout(Hl, S, R, ncw, static_cast<int32_t>(csize), p.gamma != nullptr);
     const uint32_t ring = smem_u32(smem);
     const uint32_t full0 = ring + L.bars, empty0 = full0 + 8u * S, redbar = empty0 + 8u * S;
+    const uint32_t gbar = redbar + 8u;    // the gamma copy
     const uint32_t xbar0 = redbar + 16u;  // two cross-CTA barriers, by token parity
     StageMeta *meta = reinterpret_cast<StageMeta *>(smem + L.meta);
     float *red = reinterpret_cast<float *>(smem + L.red);
@@ -209,6 +212,7 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
             mbar_init(empty0 + 8u * s, ncw);
         }
         mbar_init(redbar, ncw);
+        mbar_init(gbar, 1);
         if constexpr (SPLIT) {
             mbar_init(xbar0, csize * ncw);
             mbar_init(xbar0 + 8u, csize * ncw);
@@ -237,6 +241,10 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
             auto row_of = [&](int64_t tt) {
                 return p.slot_major ? static_cast<int32_t>(lane * p.T + tt) : __ldg(p.row_map + tt * k + lane);
             };
+            if (p.gamma && lane == 0) {
+                mbar_arrive_expect_tx(gbar, copy_bytes);
+                bulk_g2s(ring + L.gamma, p.gamma + col0, copy_bytes, gbar);
+            }
             if (t < p.T && lane < k) {
                 r_next = row_of(t);
                 w_next = load_weight(p.weights, t * k + lane, p.weight_dtype);
@@ -325,6 +333,8 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                 // a slot never freed up: record it, then let every copy this
                 // warp started land before the CTA's shared memory goes away
                 report(p.status, MOE_ERR_DEVICE_TIMEOUT);
+                if (p.gamma)
+                    mbar_wait_bounded(gbar, 0, kWaitLimitNs);
                 const int64_t nn = issued < S ? issued : S;
                 for (int64_t s = 0; s < nn; ++s) {
                     const int64_t times = (issued - 1 - s) / S + 1;
@@ -346,6 +356,11 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
             }
             const bool do_norm = p.gamma != nullptr;
             const int max_slots = k + 3;  // a token never needs more slots than rows + 1
+            // gamma's slice, copied to shared memory once by the producer
+            if (do_norm && __any_sync(0xffffffffu, !mbar_wait_bounded(gbar, 0, kWaitLimitNs))) {
+                report(p.status, MOE_ERR_DEVICE_TIMEOUT);
+                return;
+            }
 
             int stage = 0;
             uint32_t phase = 0;
@@ -435,12 +450,11 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                     }
                 }
                 if (do_norm) {
-                    // gamma is re-read per token; it stays in L1 / L2
                     uint4 gq[VPT];
 #pragma unroll
                     for (int s = 0; s < VPT; ++s) {
                         const int v = s * NC + tid;
-                        gq[s] = (v < nvec) ? __ldg(reinterpret_cast<const uint4 *>(p.gamma + col0) + v)
+                        gq[s] = (v < nvec) ? *reinterpret_cast<const uint4 *>(smem + L.gamma + 16 * v)
                                            : make_uint4(0, 0, 0, 0);
                     }
                     float ss = 0.f;
@@ -452,7 +466,8 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
 #pragma unroll
                     for (int d = 16; d > 0; d >>= 1)
                         ss += __shfl_xor_sync(0xffffffffu, ss, d);
-                    float total = 0.f;
+                    const float *part;
+                    int np;
                     if constexpr (SPLIT) {
                         // every warp of every CTA of the cluster sends its partial
                         // to slot [rank][warp] of every CTA (lane r to CTA r) and
@@ -462,7 +477,7 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                         // parity: a CTA can run at most one token ahead of a peer
                         // that has not yet read its partials.
                         const uint32_t par = tok & 1u;
-                        float *part = red + par * csize * static_cast<uint32_t>(ncw);
+                        part = red + par * csize * static_cast<uint32_t>(ncw);
                         __syncwarp();
                         if (static_cast<uint32_t>(lane) < csize) {
                             const uint32_t mine = smem_u32(part + crank * ncw + warp);
@@ -474,22 +489,30 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                             report(p.status, MOE_ERR_DEVICE_TIMEOUT);
                             return;
                         }
-                        const int np = static_cast<int>(csize) * ncw;
-                        for (int w = 0; w < np; ++w)
-                            total += part[w];
+                        np = static_cast<int>(csize) * ncw;
                     } else {
-                        float *part = red + (tok & 1u) * ncw;
+                        float *mine = red + (tok & 1u) * ncw;
                         if (lane == 0) {
-                            part[warp] = ss;
+                            mine[warp] = ss;
                             mbar_arrive(redbar);
                         }
                         if (__any_sync(0xffffffffu, !mbar_wait_bounded(redbar, tok & 1u, kWaitLimitNs))) {
                             report(p.status, MOE_ERR_DEVICE_TIMEOUT);
                             return;
                         }
-                        for (int w = 0; w < ncw; ++w)
-                            total += part[w];
+                        part = mine;
+                        np = ncw;
                     }
+                    // the partials, strided over the lanes and then added by a
+                    // butterfly: each step adds the same two values in every
+                    // lane (addition commutes), so all lanes of all warps end
+                    // with one identical total
+                    float total = 0.f;
+                    for (int w = lane; w < np; w += 32)
+                        total += part[w];
+#pragma unroll
+                    for (int d = 16; d > 0; d >>= 1)
+                        total += __shfl_xor_sync(0xffffffffu, total, d);
                     const float rinv = 1.0f / sqrtf(total / static_cast<float>(H) + p.eps);
 #pragma unroll
                     for (int s = 0; s < VPT; ++s) {
@@ -645,31 +668,17 @@ inline bool split_ok(int32_t H, int32_t quant, int c)
     return c >= 2 && c <= kMaxSplit && H % (c * blk) == 0 && H / c <= kMaxSplitCols;
 }
 
-constexpr int kMinAutoSplitCols = 256;  // one vector per lane of one full warp
-
-// CTAs per token.  One CTA per token streams a row set through one SM; with
-// fewer tokens than SMs most of the GPU would idle, so a token is spread over
-// the smallest cluster of 2, 4, 8 or 16 CTAs that gives every SM work (or the
-// largest allowed), keeping slices of at least kMinAutoSplitCols columns.
-// moe_tuning_set may force 1 or a cluster size.
-inline int choose_split(int32_t H, int64_t T, int32_t quant, int forced)
+// CTAs per token: 1 unless moe_tuning_set asks for a cluster size.  Measured
+// on GB300 (graphs of back-to-back launches, H = 7168, k = 8, T = 1..128),
+// splitting never paid: the combine at decode sizes is bound by a fixed chain
+// of latencies (launch, row_map load, row copies, epilogue), not by one SM's
+// share of HBM bandwidth, and a cluster adds its own launch and barrier cost
+// (T = 64: 5.7 us whole rows, 6.4 us in pairs, 10.1 us in clusters of 16).
+inline int choose_split(int32_t H, int64_t, int32_t quant, int forced)
 {
-    if (forced == 1)
-        return 1;
     if (forced >= 2)
         return split_ok(H, quant, forced) ? forced : 1;
-    const int sms = sm_count();
-    if (sms <= 0 || T >= sms)
-        return 1;
-    int best = 1;
-    for (int c = 2; c <= kMaxSplit && H / c >= kMinAutoSplitCols; c *= 2) {
-        if (!split_ok(H, quant, c))
-            continue;
-        best = c;
-        if (T * c >= sms)
-            break;
-    }
-    return best;
+    return 1;
 }
 
 // Whole rows (split 1): vectors per consumer thread, the smallest of 1, 2,
@@ -680,10 +689,10 @@ inline int choose_split(int32_t H, int64_t T, int32_t quant, int forced)
 // (per-row overhead); at H = 4096, 16 warps x 1 beat 8 x 2.  Ring: about
 // kDefaultRingBytes of rows, at least 2 slots, within the shared-memory
 // budget.
-// Split rows: one vector per thread over the H / split columns, and a ring
-// that holds a whole token (k + 2 rows), so that the producer never waits
-// inside a token and several CTAs fit on one SM.
-inline Plan make_plan(int32_t H, int64_t T, int32_t k, int32_t quant, int split_request)
+// Split rows (when requested): one vector per thread over the H / split
+// columns, and a ring that holds a whole token (k + 2 rows), so that the
+// producer never waits inside a token and several CTAs fit on one SM.
+inline Plan make_plan(int32_t H, int64_t T, int32_t k, int32_t quant, bool with_gamma, int split_request)
 {
     const Tuning tu = g_tuning;
     Plan pl{};
@@ -710,7 +719,7 @@ inline Plan make_plan(int32_t H, int64_t T, int32_t k, int32_t quant, int split_
     pl.ctas_per_sm = tu.ctas_per_sm ? tu.ctas_per_sm : 1;
     // one CTA keeps kSmemBudget; several share the SM's 228 KB (1 KB reserved each)
     const size_t budget = pl.ctas_per_sm == 1 ? kSmemBudget : (224 * 1024) / pl.ctas_per_sm - 2048;
-    const SmemLayout one = smem_layout(pl.hl, 1, pl.rows, pl.ncw, pl.split);
+    const SmemLayout one = smem_layout(pl.hl, 1, pl.rows, pl.ncw, pl.split, with_gamma);
     const size_t per_slot = one.slot_stride + 16 + sizeof(StageMeta);
     const size_t fixed = one.total - per_slot;
     int s;
@@ -725,7 +734,7 @@ inline Plan make_plan(int32_t H, int64_t T, int32_t k, int32_t quant, int split_
     s = s > fit ? fit : s;
     s = s > kMaxStages ? kMaxStages : s;
     pl.stages = s < 2 ? 2 : s;
-    pl.smem = smem_layout(pl.hl, pl.stages, pl.rows, pl.ncw, pl.split);
+    pl.smem = smem_layout(pl.hl, pl.stages, pl.rows, pl.ncw, pl.split, with_gamma);
     return pl;
 }
 
