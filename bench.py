@@ -283,7 +283,7 @@ def run_ours(args):
     host = {n: pinned(inp[n]) for n in names}
     flush = torch.empty(L2_FLUSH_BYTES if args.l2 == "write" else 16, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    route_kernels = 0 if kind == "slot_major" else (1 if (T * k <= 524288 and E <= 1024) else 3)
+    route_kernels = 0 if kind == "slot_major" else nqg.moe_build_row_map_launches(T, k, E)
 
     def buffer_set():
         """Device inputs, outputs and the calls of one step over them."""

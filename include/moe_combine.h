@@ -170,6 +170,14 @@ moe_status moe_build_row_map(const int32_t *topk_ids, int64_t T, int32_t top_k, 
  * MOE_ERR_INVALID_EXPERT (or MOE_ERR_CUDA if the read fails). */
 moe_status moe_build_row_map_check(const void *workspace, moe_stream_t stream);
 
+/* Kernels that moe_build_row_map(T, top_k, E) launches on the current device
+ * with the current tuning: 1 (one thread-block cluster does the histogram,
+ * scan and scatter), 3 (histogram, scan, scatter kernels over the
+ * workspace) or 0 (T == 0: only memsets).  Launches nothing.  Returns
+ * MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED as
+ * moe_build_row_map_workspace_size does.  (No counterpart on the pages.) */
+moe_status moe_build_row_map_launches(int64_t T, int32_t top_k, int32_t E, int32_t *launches);
+
 /* ------------------------------------------------------------------------
  * Routing build without a workspace (no counterpart on the pages: an
  * addition of this library for callers that cannot allocate).

@@ -68,6 +68,7 @@ SYMBOLS = {
                                     C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t,
                                     C.c_void_p]),
     "moe_build_row_map_check": (C.c_int, [C.c_void_p, C.c_void_p]),
+    "moe_build_row_map_launches": (C.c_int, [C.c_int64, C.c_int32, C.c_int32, C.POINTER(C.c_int32)]),
     "moe_build_row_map_noalloc": (C.c_int, [C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_void_p,
                                             C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     "moe_combine": (C.c_int, [C.POINTER(MoeCombineArgs), C.c_void_p]),
@@ -164,6 +165,13 @@ def moe_build_row_map_noalloc(topk_ids, E: int, counts, offsets, row_map, src_ro
 def moe_build_row_map_check(workspace, stream=None) -> int:
     """Synchronises the stream; MOE_OK or MOE_ERR_INVALID_EXPERT."""
     return int(lib().moe_build_row_map_check(_ptr(workspace), _stream(stream)))
+
+
+def moe_build_row_map_launches(T: int, top_k: int, E: int) -> int:
+    """Kernels moe_build_row_map launches for this shape on the current device (1, 3, or 0)."""
+    n = C.c_int32(-1)
+    _check(lib().moe_build_row_map_launches(T, top_k, E, C.byref(n)), "moe_build_row_map_launches")
+    return n.value
 
 
 def moe_scales_bytes(T: int, H: int, quant: str, sf_layout: str = "linear") -> int:

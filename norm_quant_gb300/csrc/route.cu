@@ -259,8 +259,8 @@ struct FusedPlan {
 
 size_t fused_smem(int32_t E)
 {
-    // hist[E][33] + all_tot[16][E] + base[E] + off[E + 1] + wsum[32]
-    return (static_cast<size_t>(kHistPitch + kFusedMaxCtas + 2) * E + 1 + 32) * sizeof(int32_t);
+    // hist[E][33] + all_tot[16][E] + base[E] + off[E + 1] + wsum[32] + the CTA's error flag
+    return (static_cast<size_t>(kHistPitch + kFusedMaxCtas + 2) * E + 1 + 32 + 1) * sizeof(int32_t);
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -301,6 +301,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     int32_t *base = all_tot + static_cast<size_t>(kFusedMaxCtas) * E;  // [E]: offsets + lower CTAs
     int32_t *off = base + E;                                          // [E + 1]
     int32_t *wsum = off + E + 1;                                      // [32]
+    int32_t &cta_bad = wsum[32];                                      // an id outside [-1, E) seen here
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const int nctas = static_cast<int>(gridDim.x);
@@ -343,11 +344,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             hist[e * kHistPitch + warp] += __popc(peers);
         __syncwarp();
     }
-    // the error word is cleared by CTA 0 before the cluster barrier and only
-    // OR-ed into after it
-    if (rank == 0 && threadIdx.x == 0)
-        *err = 0;
-    __syncthreads();
+    // whether any slot of this CTA held an id outside [-1, E); CTA 0 gathers
+    // the CTAs' flags with their totals and writes the error word once, at
+    // the end (a global store before a cluster barrier would make its
+    // release wait for the store to reach L2)
+    {
+        const int32_t b = __syncthreads_or(bad ? 1 : 0);
+        if (threadIdx.x == 0)
+            cta_bad = b;
+    }
     // 2. per expert: exclusive prefix over the 32 warp columns (a shuffle
     //    scan, kScanIlp experts at a time per warp) and the CTA's total
     for (int e0 = warp * kScanIlp; e0 < E; e0 += kFusedWarps * kScanIlp) {
@@ -377,10 +382,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
     // 3. publish the totals; every CTA pulls the other CTAs' rows (all loads
     //    in flight at once); the second barrier keeps every CTA alive until
-    //    no one reads its shared memory any more
-    cluster_sync_all();
-    if (__any_sync(0xffffffffu, bad) && lane == 0)
-        atomicOr(err, 1);
+    //    no one reads its shared memory any more.  A lone CTA needs only its
+    //    own barrier.
+    if (nctas > 1)
+        cluster_sync_all();
+    else
+        __syncthreads();
+    // CTA 0's first warp reads the CTAs' flags at once, lane b from CTA b
+    int32_t any_bad = 0;
+    if (rank == 0 && warp == 0) {
+        const int32_t f = lane >= nctas ? 0 : (lane == 0 ? cta_bad : ld_dsmem(&cta_bad, static_cast<uint32_t>(lane)));
+        any_bad = __any_sync(0xffffffffu, f != 0) ? 1 : 0;
+    }
     for (int e = threadIdx.x; e < E; e += kFusedThreads) {
         int32_t x[kFusedMaxCtas];
 #pragma unroll
@@ -391,7 +404,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             if (b < nctas && b != static_cast<int>(rank))
                 all_tot[b * E + e] = x[b];
     }
-    cluster_sync_all();
+    if (nctas > 1)
+        cluster_sync_all();
+    else
+        __syncthreads();
+    if (rank == 0 && threadIdx.x == 0)
+        *err = any_bad;
     // 4. counts, exclusive scan over experts, this CTA's base per expert
     {
         const int per_t = (E + kFusedThreads - 1) / kFusedThreads;  // 1 for E <= 1024
@@ -559,6 +577,17 @@ extern "C" moe_status moe_build_row_map_workspace_size(int64_t T, int32_t top_k,
     if (top_k > MOE_MAX_TOP_K || E > MOE_MAX_EXPERTS || T * top_k >= (int64_t(1) << 31))
         return MOE_ERR_UNSUPPORTED;
     *bytes = layout_for(T * top_k, E).total;
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_build_row_map_launches(int64_t T, int32_t top_k, int32_t E, int32_t *launches)
+{
+    if (!launches || T < 0 || top_k < 1 || E < 1)
+        return MOE_ERR_INVALID_ARG;
+    if (top_k > MOE_MAX_TOP_K || E > MOE_MAX_EXPERTS || T * top_k >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED;
+    FusedPlan f;
+    *launches = T == 0 ? 0 : (fused_plan(T * top_k, E, &f) ? 1 : 3);
     return MOE_OK;
 }
 

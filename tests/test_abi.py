@@ -123,6 +123,11 @@ def test_route_validation(L):
     assert L.moe_build_row_map(0x400, 4, 2, 8, 0x100, 0x200, 0x300, None, ws, 8, None) == 3
     assert L.moe_build_row_map(0x400, 4, 2, 8, 0x100, 0x200, 0x300, None, None, 0, None) == 3
     assert L.moe_build_row_map(0x400, 4, 2, 8, None, 0x200, 0x300, None, ws, 1 << 20, None) == 1
+    k = C.c_int32(-1)
+    assert L.moe_build_row_map_launches(10, 4, 8, None) == 1
+    assert L.moe_build_row_map_launches(-1, 4, 8, C.byref(k)) == 1
+    assert L.moe_build_row_map_launches(10, 33, 8, C.byref(k)) == 2
+    assert L.moe_build_row_map_launches(0, 4, 8, C.byref(k)) == 0 and k.value == 0
 
 
 def test_dispatch_validation(L):

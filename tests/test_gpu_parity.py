@@ -165,6 +165,21 @@ def _routing_sizes():
         assert torch.equal(a, b)
 
 
+def test_single_launch_routing_is_planned_at_the_workload_sizes():
+    """The one-cluster routing build is the plan at every workload's size
+    (a plan that silently fell back to three kernels would still pass the
+    parity tests), and route_cluster = -1 selects the three kernels."""
+    for wl in synth.WORKLOADS:
+        assert nqg.moe_build_row_map_launches(wl.T, wl.k, wl.E) == 1, wl.name
+    assert nqg.moe_build_row_map_launches(16384, 8, 256) == 1
+    assert nqg.moe_build_row_map_launches(40000, 8, 256) == 3  # beyond one cluster's slots
+    try:
+        nqg.moe_tuning_set(route_cluster=-1)
+        assert nqg.moe_build_row_map_launches(64, 8, 256) == 3
+    finally:
+        nqg.moe_tuning_set()
+
+
 def test_invalid_expert_ids_are_flagged():
     ids = np.array([[0, 1], [9, -1], [-5, 2]], np.int32)
     st, counts, offsets, row_map, _ = gpu_route(ids, 4)
