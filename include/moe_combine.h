@@ -277,8 +277,9 @@ moe_status moe_combine(const moe_combine_args *args, moe_stream_t stream);
  *   vpt            8-element vectors per consumer thread: 1, 2, 4 or 8
  *                  (ignored where it cannot cover H; at most 28, 16, 8, 8
  *                  consumer warps respectively);
- *   rows_per_slot  rows staged per ring slot, 1..4 (capped at 4 for vpt <= 2,
- *                  2 for vpt 4, 1 for vpt 8);
+ *   rows_per_slot  most rows staged per ring slot, 1..8 (a token's rows are
+ *                  spread evenly over as few slots as that allows; fewer
+ *                  where two slots would not fit in shared memory);
  *   ring_kib       shared-memory ring size in KiB, 1..224 (capped to what fits);
  *   ctas_per_sm    resident CTAs per SM the grid is sized for, 1..4;
  *   route_cluster  routing build: 0 automatic, -1 the three-kernel path,

@@ -74,7 +74,7 @@ extern "C" moe_status moe_tuning_set(int32_t vpt, int32_t rows_per_slot, int32_t
         return MOE_ERR_INVALID_ARG;
     if (!(vpt == 0 || vpt == 1 || vpt == 2 || vpt == 4 || vpt == 8))
         return MOE_ERR_INVALID_ARG;
-    if (rows_per_slot < 0 || rows_per_slot > 4 || ring_kib < 0 || ring_kib > 224 || ctas_per_sm < 0 ||
+    if (rows_per_slot < 0 || rows_per_slot > kMaxSlotRows || ring_kib < 0 || ring_kib > 224 || ctas_per_sm < 0 ||
         ctas_per_sm > 4)
         return MOE_ERR_INVALID_ARG;
     if (!(combine_split == 0 || combine_split == 1 || combine_split == 2 || combine_split == 4 ||
@@ -178,9 +178,12 @@ extern "C" moe_status moe_combine(const moe_combine_args *a, moe_stream_t stream
         p.hl = pl.hl;
         return a->io_dtype == MOE_IO_FP16 ? launch_io<1>(p, pl, a->quant, s) : launch_io<0>(p, pl, a->quant, s);
     };
-    const Plan pl = make_plan(a->H, a->T, a->top_k, a->quant, a->gamma != nullptr, g_tuning.split);
+    // rows a token may need: its valid expert rows, the shared row, the residual row
+    const int rows_per_token = a->top_k + (a->shared_out ? 1 : 0) + (a->residual ? 1 : 0);
+    const bool with_gamma = a->gamma != nullptr;
+    const Plan pl = make_plan(a->H, a->T, rows_per_token, a->quant, with_gamma, g_tuning.split);
     const moe_status st = launch(pl);
-    if (st == MOE_ERR_UNSUPPORTED && pl.split > 1)
-        return launch(make_plan(a->H, a->T, a->top_k, a->quant, a->gamma != nullptr, 1));  // no room for the cluster: whole rows
+    if (st == MOE_ERR_UNSUPPORTED && pl.split > 1)  // no room for the cluster: whole rows
+        return launch(make_plan(a->H, a->T, rows_per_token, a->quant, with_gamma, 1));
     return st;
 }

@@ -23,19 +23,20 @@ constexpr size_t kDefaultRingBytes = 144 * 1024;
 template <int VPT>
 __host__ __device__ constexpr int max_consumer_warps() { return VPT <= 2 ? 16 : 8; }
 inline int max_consumer_warps_rt(int vpt) { return vpt <= 2 ? 16 : 8; }
-// Rows a ring slot may hold, bounded by the registers the loads take.
+// Rows a consumer loads into registers at once (its chunk of a slot),
+// bounded by the registers the loads take; a slot holds up to kMaxSlotRows.
 template <int VPT>
-__host__ __device__ constexpr int max_rows() { return VPT <= 2 ? 4 : (VPT == 4 ? 2 : 1); }
-inline int max_rows_rt(int vpt) { return vpt <= 2 ? 4 : (vpt == 4 ? 2 : 1); }
+__host__ __device__ constexpr int chunk_rows() { return VPT <= 2 ? 4 : (VPT == 4 ? 2 : 1); }
+constexpr int kMaxSlotRows = 8;
 
 enum : int32_t { F_LAST = 1, F_RESID = 2 };
 
-struct StageMeta {
+struct alignas(16) StageMeta {
     int32_t t;
     int32_t n;      // rows in the slot, 0..R
     int32_t flags;  // F_LAST: the token's last slot; F_RESID: its last row is the residual
     int32_t pad;
-    float w[4];     // weight of each row (1 for the shared and residual rows)
+    float w[kMaxSlotRows];  // weight of each row (1 for the shared and residual rows)
 };
 
 struct Params {
@@ -172,10 +173,51 @@ __device__ __forceinline__ int32_t ue8m0_fp4_byte(float amax)
     return b < 0 ? 0 : (b > 254 ? 254 : b);
 }
 
+// N consecutive slot weights from shared memory (16-byte aligned for N = 4,
+// 8-byte for N = 2) in one load.
+template <int N>
+__device__ __forceinline__ void load_weights(const float *w, float *out)
+{
+    if constexpr (N == 4) {
+        const float4 x = *reinterpret_cast<const float4 *>(w);
+        out[0] = x.x;
+        out[1] = x.y;
+        out[2] = x.z;
+        out[3] = x.w;
+    } else if constexpr (N == 2) {
+        const float2 x = *reinterpret_cast<const float2 *>(w);
+        out[0] = x.x;
+        out[1] = x.y;
+    } else {
+        out[0] = w[0];
+    }
+}
+
+// Position of the set bit of `mask` that has `rank` set bits below it
+// (rank < popc(mask)), by halving the search window: skip the low half of the
+// window when it holds no more than `rank` set bits.  A result whose bit is
+// not set (impossible for a valid rank) is replaced by the lowest set bit, so
+// the lane it names always holds a valid row.
+__device__ __forceinline__ int nth_set_bit(uint32_t mask, int rank)
+{
+    uint32_t m = mask;
+    int pos = 0;
+#pragma unroll
+    for (int b = 16; b >= 1; b >>= 1) {
+        const int c = __popc(m & ((1u << b) - 1u));
+        if (c <= rank) {
+            rank -= c;
+            m >>= b;
+            pos += b;
+        }
+    }
+    return ((mask >> pos) & 1u) ? pos : (mask ? __ffs(mask) - 1 : 0);
+}
+
 template <int VPT, int QUANT, int IO, bool SPLIT>
 __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combine_kernel(const Params p)
 {
-    constexpr int RMAX = max_rows<VPT>();
+    constexpr int RCH = chunk_rows<VPT>();
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ncw = (blockDim.x >> 5) - 1;
@@ -262,64 +304,64 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                     report(p.status, MOE_ERR_ROW_OUT_OF_RANGE);
                     valid = false;
                 }
-                uint32_t mrem = __ballot_sync(0xffffffffu, valid);
-                const int n_exp = __popc(mrem);
+                const uint32_t mval = __ballot_sync(0xffffffffu, valid);
+                const int n_exp = __popc(mval);
                 const bool has_sh = p.shared != nullptr, has_res = p.residual != nullptr;
                 const int n = n_exp + (has_sh ? 1 : 0) + (has_res ? 1 : 0);
-                int i = 0;
-                do {  // one ring slot per iteration; a token with no rows still gets one
-                    const int ns = (n - i < R) ? n - i : R;
-                    const uint8_t *src[RMAX];
-                    float wt[RMAX];
-#pragma unroll
-                    for (int q = 0; q < RMAX; ++q) {
-                        src[q] = nullptr;
-                        wt[q] = 1.f;
-                        const int ii = i + q;
-                        if (q < ns) {  // warp-uniform
-                            if (ii < n_exp) {
-                                const int j = __ffs(mrem) - 1;
-                                mrem &= mrem - 1;
-                                const int32_t rj = __shfl_sync(0xffffffffu, r, j);
-                                wt[q] = __shfl_sync(0xffffffffu, w, j);
-                                src[q] = p.expert_out + static_cast<int64_t>(rj) * row_bytes + col_bytes;
-                            } else if (has_sh && ii == n_exp) {
-                                src[q] = p.shared + t * row_bytes + col_bytes;
-                            } else {
-                                src[q] = p.residual + t * row_bytes + col_bytes;
-                            }
-                        }
+                // the token's rows spread evenly over ceil(n / R) slots (9 rows
+                // at R = 4 as 3 + 3 + 3, not 4 + 4 + 1); a token with no rows
+                // still gets one slot
+                const int nslots = n > 0 ? (n + R - 1) / R : 1;
+                int i = 0, si = 0;
+                do {
+                    const int left = nslots - si;
+                    const int ns = (n - i + left - 1) / left;
+                    // lane q stages row i + q: the (i + q)-th valid expert slot in
+                    // ascending j, then the shared row, then the residual row
+                    const int ii = i + lane;
+                    const bool mine = lane < ns;
+                    const int j = nth_set_bit(mval, ii < n_exp ? ii : 0);
+                    const int32_t rj = __shfl_sync(0xffffffffu, r, j);
+                    const float wj = __shfl_sync(0xffffffffu, w, j);
+                    const uint8_t *src = nullptr;
+                    if (mine) {
+                        if (ii < n_exp)
+                            src = p.expert_out + static_cast<int64_t>(rj) * row_bytes + col_bytes;
+                        else if (has_sh && ii == n_exp)
+                            src = p.shared + t * row_bytes + col_bytes;
+                        else
+                            src = p.residual + t * row_bytes + col_bytes;
                     }
                     const bool last = (i + ns >= n);
                     bool good = true;
-                    if (lane == 0) {
+                    if (lane == 0)
                         good = mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, kWaitLimitNs);
-                        if (good) {
-                            StageMeta &m = meta[stage];
-                            m.t = static_cast<int32_t>(t);
-                            m.n = ns;
-                            m.flags = (last ? F_LAST : 0) | ((last && has_res && ns > 0) ? F_RESID : 0);
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                m.w[q] = q < RMAX ? wt[q < RMAX ? q : 0] : 1.f;
-                            const uint32_t full = full0 + 8u * stage;
-                            if (ns > 0) {
-                                mbar_arrive_expect_tx(full, static_cast<uint32_t>(ns) * copy_bytes);
-                                const uint32_t dst = ring + static_cast<uint32_t>(stage) * L.slot_stride;
-#pragma unroll
-                                for (int q = 0; q < RMAX; ++q)
-                                    if (q < ns)
-                                        bulk_g2s(dst + static_cast<uint32_t>(q) * L.row_stride, src[q], copy_bytes,
-                                                 full);
-                            } else {
-                                mbar_arrive(full);
-                            }
-                        }
-                    }
                     good = __shfl_sync(0xffffffffu, good, 0);
                     if (!good) {
                         ok = false;
                         break;
+                    }
+                    // each lane copies its own row and records its weight; lane 0
+                    // then publishes the slot and arms its barrier.  Until lane
+                    // 0 arrives the phase has an arrival pending, so copies that
+                    // land before the expected bytes are set cannot complete it.
+                    const uint32_t full = full0 + 8u * stage;
+                    StageMeta &m = meta[stage];
+                    if (mine) {
+                        m.w[lane] = ii < n_exp ? wj : 1.f;
+                        bulk_g2s(ring + static_cast<uint32_t>(stage) * L.slot_stride +
+                                     static_cast<uint32_t>(lane) * L.row_stride,
+                                 src, copy_bytes, full);
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        m.t = static_cast<int32_t>(t);
+                        m.n = ns;
+                        m.flags = (last ? F_LAST : 0) | ((last && has_res && ns > 0) ? F_RESID : 0);
+                        if (ns > 0)
+                            mbar_arrive_expect_tx(full, static_cast<uint32_t>(ns) * copy_bytes);
+                        else
+                            mbar_arrive(full);
                     }
                     ++issued;
                     if (++stage == S) {
@@ -327,6 +369,7 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                         phase ^= 1u;
                     }
                     i += ns;
+                    ++si;
                 } while (i < n);
             }
             if (!ok && lane == 0) {
@@ -380,42 +423,57 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                         report(p.status, MOE_ERR_DEVICE_TIMEOUT);
                         return;
                     }
-                    const StageMeta m = meta[stage];
+                    // the slot's header (t, n, flags) in one 16-byte load
+                    const int4 hdr = *reinterpret_cast<const int4 *>(&meta[stage]);
+                    const int mn = hdr.y, mflags = hdr.z;
                     const uint8_t *slot = smem + static_cast<uint32_t>(stage) * L.slot_stride;
-                    uint4 q[RMAX][VPT];
+                    // the slot's rows in chunks of RCH: all of a chunk's loads
+                    // first, then its sums in row order
 #pragma unroll
-                    for (int rr = 0; rr < RMAX; ++rr)
-#pragma unroll
-                        for (int s = 0; s < VPT; ++s) {
-                            const int v = s * NC + tid;
-                            q[rr][s] = make_uint4(0, 0, 0, 0);
-                            if (rr < m.n && v < nvec)
-                                q[rr][s] = *reinterpret_cast<const uint4 *>(slot + rr * L.row_stride + 16 * v);
-                        }
-#pragma unroll
-                    for (int rr = 0; rr < RMAX; ++rr) {
-                        if (rr >= m.n)
+                    for (int c0 = 0; c0 < kMaxSlotRows; c0 += RCH) {
+                        if (c0 >= mn)
                             break;
-                        if ((m.flags & F_RESID) && rr == m.n - 1 && p.combined_out) {
+                        uint4 q[RCH][VPT];
+                        // the chunk's weights in one vector load (beyond the
+                        // slot's rows they are stale and unused)
+                        float wr[RCH];
+                        load_weights<RCH>(meta[stage].w + c0, wr);
+#pragma unroll
+                        for (int rr = 0; rr < RCH; ++rr) {
+                            const int row = c0 + rr;
 #pragma unroll
                             for (int s = 0; s < VPT; ++s) {
                                 const int v = s * NC + tid;
-                                if (v < nvec)
-                                    store16x8<IO>(p.combined_out, t * H + col0 + 8 * v, acc[s]);
+                                q[rr][s] = make_uint4(0, 0, 0, 0);
+                                if (row < mn && v < nvec)
+                                    q[rr][s] = *reinterpret_cast<const uint4 *>(slot + row * L.row_stride + 16 * v);
                             }
-                            combined_done = true;
                         }
-                        const float wr = m.w[rr];
 #pragma unroll
-                        for (int s = 0; s < VPT; ++s) {
-                            const int v = s * NC + tid;
-                            if (v < nvec) {
-                                const uint32_t qw[4] = {q[rr][s].x, q[rr][s].y, q[rr][s].z, q[rr][s].w};
+                        for (int rr = 0; rr < RCH; ++rr) {
+                            const int row = c0 + rr;
+                            if (row >= mn)
+                                break;
+                            if ((mflags & F_RESID) && row == mn - 1 && p.combined_out) {
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    float lo, hi;
-                                    unpack16x2<IO>(qw[i], lo, hi);
-                                    fma2(acc[s][2 * i], acc[s][2 * i + 1], lo, hi, wr);
+                                for (int s = 0; s < VPT; ++s) {
+                                    const int v = s * NC + tid;
+                                    if (v < nvec)
+                                        store16x8<IO>(p.combined_out, t * H + col0 + 8 * v, acc[s]);
+                                }
+                                combined_done = true;
+                            }
+#pragma unroll
+                            for (int s = 0; s < VPT; ++s) {
+                                const int v = s * NC + tid;
+                                if (v < nvec) {
+                                    const uint32_t qw[4] = {q[rr][s].x, q[rr][s].y, q[rr][s].z, q[rr][s].w};
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i) {
+                                        float lo, hi;
+                                        unpack16x2<IO>(qw[i], lo, hi);
+                                        fma2(acc[s][2 * i], acc[s][2 * i + 1], lo, hi, wr[rr]);
+                                    }
                                 }
                             }
                         }
@@ -427,7 +485,7 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                         stage = 0;
                         phase ^= 1u;
                     }
-                    if (m.flags & F_LAST)
+                    if (mflags & F_LAST)
                         break;
                 }
 
@@ -682,17 +740,20 @@ inline int choose_split(int32_t H, int64_t, int32_t quant, int forced)
 }
 
 // Whole rows (split 1): vectors per consumer thread, the smallest of 1, 2,
-// 4, 8 that needs at most 16 consumer warps.  Rows per ring slot: as many as
-// the registers allow (4 for VPT <= 2).  Measured on GB300: at H = 7168, 14
-// warps x 2 vectors with 4 rows per slot reach 93 % of HBM copy bandwidth,
-// against 73 % for 7 warps x 4 (latency-bound) and 80 % for 28 warps x 1
-// (per-row overhead); at H = 4096, 16 warps x 1 beat 8 x 2.  Ring: about
-// kDefaultRingBytes of rows, at least 2 slots, within the shared-memory
-// budget.
+// 4, 8 that needs at most 16 consumer warps.  Measured on GB300: at H = 7168,
+// 14 warps x 2 vectors reach 93 % of HBM copy bandwidth against 73 % for 7
+// warps x 4 (latency-bound) and 80 % for 28 warps x 1 (per-row overhead); at
+// H = 4096, 16 warps x 1 beat 8 x 2.  Rows per ring slot: the fewest slots
+// per token that leave room for three slots (measured, Gemma NVFP4 at
+// H = 4096, 9 rows a token: 5 rows a slot 0.84 of copy bandwidth, 3 rows 0.77,
+// 8 rows with only two slots 0.79; prefill at H = 7168, 10 rows: 4 rows 0.98,
+// 5 rows with two slots 0.96).  Ring: about kDefaultRingBytes of rows, at
+// least 3 slots where they fit, within the shared-memory budget.
 // Split rows (when requested): one vector per thread over the H / split
-// columns, and a ring that holds a whole token (k + 2 rows), so that the
-// producer never waits inside a token and several CTAs fit on one SM.
-inline Plan make_plan(int32_t H, int64_t T, int32_t k, int32_t quant, bool with_gamma, int split_request)
+// columns, and a ring that holds a whole token, so that the producer never
+// waits inside a token and several CTAs fit on one SM.
+inline Plan make_plan(int32_t H, int64_t T, int32_t rows_per_token, int32_t quant, bool with_gamma,
+                      int split_request)
 {
     const Tuning tu = g_tuning;
     Plan pl{};
@@ -714,21 +775,40 @@ inline Plan make_plan(int32_t H, int64_t T, int32_t k, int32_t quant, bool with_
         }
     }
     pl.ncw = (nvec + 32 * pl.vpt - 1) / (32 * pl.vpt);
-    const int rmax = max_rows_rt(pl.vpt);
-    pl.rows = tu.rows ? (tu.rows < rmax ? tu.rows : rmax) : rmax;
     pl.ctas_per_sm = tu.ctas_per_sm ? tu.ctas_per_sm : 1;
     // one CTA keeps kSmemBudget; several share the SM's 228 KB (1 KB reserved each)
     const size_t budget = pl.ctas_per_sm == 1 ? kSmemBudget : (224 * 1024) / pl.ctas_per_sm - 2048;
-    const SmemLayout one = smem_layout(pl.hl, 1, pl.rows, pl.ncw, pl.split, with_gamma);
+    if (tu.rows) {
+        pl.rows = tu.rows < kMaxSlotRows ? tu.rows : kMaxSlotRows;
+    } else {
+        // as few slots per token as still leave room for three slots in the
+        // ring: each slot costs the consumers a wait and a release, and
+        // three let the producer stay a slot ahead of the one being summed
+        pl.rows = 1;
+        for (int ns = 1; ns <= rows_per_token; ++ns) {
+            const int r = (rows_per_token + ns - 1) / ns;
+            if (r <= kMaxSlotRows && smem_layout(pl.hl, 3, r, pl.ncw, pl.split, with_gamma).total <= budget) {
+                pl.rows = r;
+                break;
+            }
+        }
+    }
+    // fewer rows per slot where two slots would not fit
+    SmemLayout one = smem_layout(pl.hl, 1, pl.rows, pl.ncw, pl.split, with_gamma);
+    while (pl.rows > 1 && one.total + one.slot_stride + 16 + sizeof(StageMeta) > budget) {
+        --pl.rows;
+        one = smem_layout(pl.hl, 1, pl.rows, pl.ncw, pl.split, with_gamma);
+    }
     const size_t per_slot = one.slot_stride + 16 + sizeof(StageMeta);
     const size_t fixed = one.total - per_slot;
     int s;
     if (tu.ring_kib) {
         s = static_cast<int>((static_cast<size_t>(tu.ring_kib) * 1024 + one.slot_stride / 2) / one.slot_stride);
     } else if (pl.split > 1) {
-        s = (k + 2 + pl.rows - 1) / pl.rows;
+        s = (rows_per_token + pl.rows - 1) / pl.rows;
     } else {
         s = static_cast<int>((kDefaultRingBytes + one.slot_stride / 2) / one.slot_stride);
+        s = s < 3 ? 3 : s;
     }
     const int fit = budget > fixed ? static_cast<int>((budget - fixed) / per_slot) : 0;
     s = s > fit ? fit : s;
