@@ -277,7 +277,7 @@ moe_status moe_combine(const moe_combine_args *args, moe_stream_t stream);
  *   vpt            8-element vectors per consumer thread: 1, 2, 4 or 8
  *                  (ignored where it cannot cover H; at most 28, 16, 8, 8
  *                  consumer warps respectively);
- *   rows_per_slot  most rows staged per ring slot, 1..8 (a token's rows are
+ *   rows_per_slot  most rows staged per ring slot, 1..12 (a token's rows are
  *                  spread evenly over as few slots as that allows; fewer
  *                  where two slots would not fit in shared memory);
  *   ring_kib       shared-memory ring size in KiB, 1..224 (capped to what fits);

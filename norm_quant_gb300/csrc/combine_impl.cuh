@@ -27,7 +27,7 @@ inline int max_consumer_warps_rt(int vpt) { return vpt <= 2 ? 16 : 8; }
 // bounded by the registers the loads take; a slot holds up to kMaxSlotRows.
 template <int VPT>
 __host__ __device__ constexpr int chunk_rows() { return VPT <= 2 ? 4 : (VPT == 4 ? 2 : 1); }
-constexpr int kMaxSlotRows = 8;
+constexpr int kMaxSlotRows = 12;
 
 enum : int32_t { F_LAST = 1, F_RESID = 2 };
 

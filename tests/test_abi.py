@@ -94,7 +94,7 @@ def test_combine_validation(L, kw, want):
 
 def test_tuning_validation(L):
     assert L.moe_tuning_set(3, 0, 0, 0, 0, 0) == 1
-    assert L.moe_tuning_set(0, 9, 0, 0, 0, 0) == 1
+    assert L.moe_tuning_set(0, 13, 0, 0, 0, 0) == 1
     assert L.moe_tuning_set(0, 0, 300, 0, 0, 0) == 1
     assert L.moe_tuning_set(0, 0, 0, 9, 0, 0) == 1
     assert L.moe_tuning_set(0, 0, 0, 0, 17, 0) == 1

@@ -230,7 +230,8 @@ def test_repeat_runs_identical_and_side_stream():
 
 @pytest.mark.parametrize("plan", [(1, 1, 0, 0), (1, 4, 0, 0), (2, 1, 0, 0), (2, 4, 32, 0), (4, 1, 0, 0),
                                   (4, 2, 200, 0), (8, 1, 0, 0), (2, 2, 64, 2), (2, 2, 16, 3),
-                                  (2, 8, 0, 0), (1, 5, 0, 0), (4, 6, 0, 0), (8, 8, 0, 0), (2, 3, 0, 0)],
+                                  (2, 8, 0, 0), (1, 5, 0, 0), (4, 6, 0, 0), (8, 8, 0, 0), (2, 3, 0, 0),
+                                  (1, 12, 0, 0), (2, 9, 0, 0)],
                          ids=lambda p: "vpt%d_rows%d_ring%d_cta%d" % p)
 def test_every_launch_plan_matches_the_oracle(plan):
     """moe_tuning_set changes only how the work is laid out on the GPU."""
