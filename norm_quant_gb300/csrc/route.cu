@@ -481,6 +481,165 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
 }
 
+// Small builds (N <= kSmallMaxSlots, decode-sized batches): one CTA of 8
+// warps, launched as a plain kernel.  Warp w owns the PL * 32 consecutive
+// slots from w * PL * 32 and ranks them with ballots as above; one thread per
+// expert turns the 8 warp columns into exclusive prefixes and the expert's
+// count; a block scan over the experts gives the offsets.  The error word is
+// written once, at the end.
+constexpr int kSmallThreads = 256;
+constexpr int kSmallWarps = kSmallThreads / 32;
+constexpr int kSmallPitch = kSmallWarps + 1;  // hist[e][w] at e * 9 + w
+constexpr int kSmallMaxPerLane = 8;
+constexpr int64_t kSmallMaxSlots = int64_t(kSmallThreads) * kSmallMaxPerLane;
+constexpr int kSmallMaxExperts = 1024;
+
+size_t small_smem(int32_t E)
+{
+    // hist[E][9] + off[E] + wsum[8]
+    return (static_cast<size_t>(kSmallPitch + 1) * E + kSmallWarps) * sizeof(int32_t);
+}
+
+template <int PL>
+__global__ void __launch_bounds__(kSmallThreads, 1)
+    route_small_kernel(const int32_t *__restrict__ ids, int64_t N, int32_t E, int32_t *__restrict__ counts,
+                       int32_t *__restrict__ offsets, int32_t *__restrict__ row_map,
+                       int32_t *__restrict__ src_row, int32_t *__restrict__ err)
+{
+    extern __shared__ int32_t sh[];
+    int32_t *hist = sh;                            // [E][9]: warp counts, then prefixes
+    int32_t *off = hist + static_cast<size_t>(kSmallPitch) * E;  // [E]: counts, then offsets
+    int32_t *wsum = off + E;                       // [8]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t first = static_cast<int64_t>(warp) * (PL * 32);
+    const uint32_t lt = (1u << lane) - 1u;
+    allow_dependent_launch();  // the combine may start its setup now
+
+    // 1. ranks within each warp's slots, counts in the warp's column
+    for (int e = lane; e < E; e += 32)
+        hist[e * kSmallPitch + warp] = 0;
+    int32_t v[PL], rk[PL];
+#pragma unroll
+    for (int it = 0; it < PL; ++it) {
+        const int64_t i = first + it * 32 + lane;
+        v[it] = (i < N) ? __ldg(ids + i) : -1;
+    }
+    const int key_bits = 32 - __clz(E);
+    __syncwarp();
+    bool bad = false;
+#pragma unroll
+    for (int it = 0; it < PL; ++it) {
+        const int32_t e = v[it];
+        const bool valid = e >= 0 && e < E;
+        bad |= !valid && e != -1;
+        const uint32_t key = valid ? static_cast<uint32_t>(e) : static_cast<uint32_t>(E);
+        uint32_t peers = 0xffffffffu;
+        for (int b = 0; b < key_bits; ++b) {
+            const bool bit = (key >> b) & 1u;
+            const uint32_t on = __ballot_sync(0xffffffffu, bit);
+            peers &= bit ? on : ~on;
+        }
+        rk[it] = valid ? hist[e * kSmallPitch + warp] + __popc(peers & lt) : 0;
+        __syncwarp();
+        if (valid && (peers & lt) == 0)
+            hist[e * kSmallPitch + warp] += __popc(peers);
+        __syncwarp();
+    }
+    const int32_t any_bad = __syncthreads_or(bad ? 1 : 0);
+
+    // 2. per expert (a contiguous run of experts per thread): exclusive
+    //    prefix over the warp columns, and the count
+    const int per_t = (E + kSmallThreads - 1) / kSmallThreads;
+    const int ea = tid * per_t, eb = (ea + per_t < E) ? ea + per_t : E;
+    int32_t s = 0;
+    for (int e = ea; e < eb; ++e) {
+        int32_t c = 0;
+#pragma unroll
+        for (int w = 0; w < kSmallWarps; ++w) {
+            const int32_t x = hist[e * kSmallPitch + w];
+            hist[e * kSmallPitch + w] = c;
+            c += x;
+        }
+        off[e] = c;
+        s += c;
+    }
+    // 3. exclusive scan of the counts over the experts
+    int32_t incl = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d)
+            incl += o;
+    }
+    if (lane == 31)
+        wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int32_t ws = lane < kSmallWarps ? wsum[lane] : 0;
+        int32_t wi = ws;
+#pragma unroll
+        for (int d = 1; d < kSmallWarps; d <<= 1) {
+            const int32_t o = __shfl_up_sync(0xffffffffu, wi, d);
+            if (lane >= d)
+                wi += o;
+        }
+        if (lane < kSmallWarps)
+            wsum[lane] = wi - ws;
+        if (lane == kSmallWarps - 1) {
+            offsets[E] = wi;
+            *err = any_bad;
+        }
+    }
+    __syncthreads();
+    int32_t run = wsum[warp] + incl - s;
+    for (int e = ea; e < eb; ++e) {
+        const int32_t c = off[e];
+        counts[e] = c;
+        offsets[e] = run;
+        off[e] = run;
+        run += c;
+    }
+    __syncthreads();
+    // 4. scatter: row = offset + lower warps + rank
+#pragma unroll
+    for (int it = 0; it < PL; ++it) {
+        const int64_t i = first + it * 32 + lane;
+        const int32_t e = v[it];
+        if (e >= 0 && e < E) {
+            const int32_t row = off[e] + hist[e * kSmallPitch + warp] + rk[it];
+            row_map[i] = row;
+            if (src_row)
+                src_row[row] = static_cast<int32_t>(i);
+        } else if (i < N) {
+            row_map[i] = -1;
+        }
+    }
+}
+
+using SmallFn = decltype(&route_small_kernel<1>);
+
+// Slots per lane of the small build for N slots, or 0 where it does not
+// apply (too many slots or experts, or a routing path chosen by tuning).
+int small_plan(int64_t N, int32_t E)
+{
+    if (N > kSmallMaxSlots || E > kSmallMaxExperts || g_route_cluster != 0)
+        return 0;
+    int pl = 1;
+    while (int64_t(kSmallThreads) * pl < N)
+        pl *= 2;
+    return pl;
+}
+
+SmallFn small_fn(int per_lane)
+{
+    switch (per_lane) {
+    case 1: return route_small_kernel<1>;
+    case 2: return route_small_kernel<2>;
+    case 4: return route_small_kernel<4>;
+    default: return route_small_kernel<8>;
+    }
+}
+
 using FusedFn = void (*)(const int32_t *, int64_t, int32_t, int32_t *, int32_t *, int32_t *, int32_t *, int32_t *);
 
 FusedFn fused_fn(int per_lane)
@@ -587,7 +746,7 @@ extern "C" moe_status moe_build_row_map_launches(int64_t T, int32_t top_k, int32
     if (top_k > MOE_MAX_TOP_K || E > MOE_MAX_EXPERTS || T * top_k >= (int64_t(1) << 31))
         return MOE_ERR_UNSUPPORTED;
     FusedPlan f;
-    *launches = T == 0 ? 0 : (fused_plan(T * top_k, E, &f) ? 1 : 3);
+    *launches = T == 0 ? 0 : ((small_plan(T * top_k, E) || fused_plan(T * top_k, E, &f)) ? 1 : 3);
     return MOE_OK;
 }
 
@@ -625,6 +784,11 @@ extern "C" moe_status moe_build_row_map(const int32_t *topk_ids, int64_t T, int3
             return MOE_ERR_CUDA;
         return MOE_OK;
     }
+    if (const int pl = small_plan(N, E)) {
+        small_fn(pl)<<<1, kSmallThreads, small_smem(E), s>>>(topk_ids, N, E, counts, offsets, row_map, src_row,
+                                                              err);
+        return launch_status();
+    }
     FusedPlan f;
     if (fused_plan(N, E, &f)) {
         cudaLaunchConfig_t cfg = {};
@@ -638,7 +802,7 @@ extern "C" moe_status moe_build_row_map(const int32_t *topk_ids, int64_t T, int3
         cfg.dynamicSmemBytes = f.smem;
         cfg.stream = s;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = f.ctas > 1 ? 1 : 0;  // a lone CTA is launched as a plain kernel
         if (cudaLaunchKernelEx(&cfg, fused_fn(f.per_lane), topk_ids, N, E, counts, offsets, row_map, src_row,
                                err) != cudaSuccess) {
             cudaGetLastError();

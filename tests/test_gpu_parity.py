@@ -155,10 +155,12 @@ def test_routing_paths_and_determinism(cluster):
 
 def _routing_sizes():
     rng = np.random.Generator(np.random.PCG64(6))
-    # single-launch cluster path and (E > 1024 or N > 262144) the three-kernel path
+    # the one-CTA path (T * k <= 2048, E <= 1024, automatic plan), the
+    # single-launch cluster path and (E > 512 or N > 262144) the three-kernel path
     for T, k, E in [(1, 1, 1), (3, 2, 8192), (1000, 32, 5), (5000, 8, 1024), (70000, 2, 3),
                     (40000, 8, 256), (33000, 8, 16), (2000, 8, 2048), (32768, 8, 256),
-                    (16384, 8, 256), (70000, 8, 64)]:
+                    (16384, 8, 256), (70000, 8, 64), (64, 8, 256), (256, 8, 256), (257, 8, 256),
+                    (200, 10, 1024), (7, 3, 1), (97, 1, 33), (128, 16, 1000)]:
         ids = rng.integers(-1, E, (T, k)).astype(np.int32)
         a = route_and_check(ids, E)[0]
         b = gpu_route(ids, E)[3]
@@ -178,6 +180,15 @@ def test_single_launch_routing_is_planned_at_the_workload_sizes():
         assert nqg.moe_build_row_map_launches(64, 8, 256) == 3
     finally:
         nqg.moe_tuning_set()
+
+
+def test_routing_duplicate_heavy_small_builds_match_the_oracle():
+    """Small builds where most slots share one expert (long runs of equal
+    keys within and across warps of the one-CTA kernel)."""
+    rng = np.random.Generator(np.random.PCG64(61))
+    for T, k, E in [(256, 8, 4), (100, 8, 2), (2048 // 8, 8, 1024)]:
+        ids = np.where(rng.random((T, k)) < 0.9, 1 % E, rng.integers(-1, E, (T, k))).astype(np.int32)
+        route_and_check(ids, E)
 
 
 def test_invalid_expert_ids_are_flagged():
