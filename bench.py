@@ -57,10 +57,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", choices=["tiny", "decode", "prefill", "gemma", "padded",
-                                           "slot_major", "dispatch"],
+                                           "slot_major", "dispatch", "mxfp4", "fp16"],
                     default="prefill", help="the headline is prefill; the others are for analysis "
                     "(slot_major: the prefill shape with [k, T, H] expert rows; dispatch: the "
-                    "prefill shape's dispatch-side permute)")
+                    "prefill shape's dispatch-side permute; mxfp4: the prefill shape with MXFP4 "
+                    "output; fp16: the prefill shape with fp16 inputs, outputs and router weights)")
     ap.add_argument("--l2", choices=["none", "write"], default="none",
                     help="none: inputs larger than L2; write: 256 MB write before each step")
     return ap.parse_args()
@@ -90,10 +91,14 @@ def dist_env():
 
 
 def workload(name="prefill"):
+    import dataclasses
     from norm_quant_gb300 import synth
-    return {"tiny": synth.TINY, "decode": synth.DECODE, "prefill": synth.PREFILL,
-            "gemma": synth.GEMMA_NVFP4, "padded": synth.PADDED, "slot_major": synth.PREFILL,
-            "dispatch": synth.PREFILL}[name]
+    P = synth.PREFILL
+    return {"tiny": synth.TINY, "decode": synth.DECODE, "prefill": P,
+            "gemma": synth.GEMMA_NVFP4, "padded": synth.PADDED, "slot_major": P, "dispatch": P,
+            "mxfp4": dataclasses.replace(P, quant="mxfp4", name=P.name.replace("mxfp8", "mxfp4")),
+            "fp16": dataclasses.replace(P, io_dtype="fp16", weight_dtype="fp16",
+                                        name=P.name.replace("rmsnorm", "fp16io_fp16weights_rmsnorm"))}[name]
 
 
 def algorithmic_bytes(wl, n_valid: int) -> dict:
@@ -101,12 +106,15 @@ def algorithmic_bytes(wl, n_valid: int) -> dict:
     T, H, k = wl.T, wl.H, wl.k
     rows = n_valid * 2 * H
     other = (2 * H * T if wl.shared_std is not None else 0) + (2 * H * T if wl.residual else 0)
-    meta = 8 * k * T + (2 * H if wl.gamma_mean is not None else 0)
+    weight_bytes = 4 if wl.weight_dtype == "fp32" else 2
+    meta = (4 + weight_bytes) * k * T + (2 * H if wl.gamma_mean is not None else 0)
     writes = 2 * H * T * len([o for o in wl.outputs if o in ("combined", "residual", "norm")])
     if wl.quant == "mxfp8":
         writes += H * T + H // 32 * T
     elif wl.quant == "nvfp4":
         writes += H // 2 * T + H // 16 * T
+    elif wl.quant == "mxfp4":
+        writes += H // 2 * T + H // 32 * T
     return {"rows": rows, "other_reads": other, "meta": meta, "writes": writes,
             "total": rows + other + meta + writes}
 
@@ -401,7 +409,8 @@ def run_ours(args):
                 sf_layout=wl.sf_layout, global_scale=1.0, combined_out=b.outs.get("combined"),
                 residual_out=b.outs.get("residual"), norm_out=b.outs.get("norm"), quant_out=b.outs.get("quant"),
                 scales_out=b.outs.get("scales"), H=H,
-                expert_layout="slot_major" if kind == "slot_major" else "grouped")
+                expert_layout="slot_major" if kind == "slot_major" else "grouped",
+                io_dtype=wl.io_dtype, weight_dtype=wl.weight_dtype)
 
         def route(st):
             if kind != "slot_major":
@@ -544,7 +553,8 @@ def run_ours(args):
             "data": "synthetic",
             "config": {"workload": wl.name, "T": T, "H": H, "E": E, "top_k": k,
                        "io": ("bf16 token rows copied to expert-grouped rows" if kind == "dispatch" else
-                              f"bf16 in, fp32 accumulate, out: {'+'.join(wl.outputs)}"
+                              f"{wl.io_dtype} in ({wl.weight_dtype} router weights), fp32 accumulate, "
+                              f"out: {'+'.join(wl.outputs)}"
                               + (f" ({wl.quant}, {wl.sf_layout} scales)" if wl.quant else "")
                               + (", slot-major [k, T, H] expert rows" if kind == "slot_major" else "")),
                        "l2": ("256 MB L2 write-flush before each step, outside the timed events"
