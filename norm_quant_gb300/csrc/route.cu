@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 constexpr int kSmallThreads = 256;
 constexpr int kSmallWarps = kSmallThreads / 32;
 constexpr int kSmallPitch = kSmallWarps + 1;  // hist[e][w] at e * 9 + w
-constexpr int kSmallMaxPerLane = 8;
+constexpr int kSmallMaxPerLane = 8;  // measured: at 4096 slots (16 a lane) a 16-CTA cluster is faster
 constexpr int64_t kSmallMaxSlots = int64_t(kSmallThreads) * kSmallMaxPerLane;
 constexpr int kSmallMaxExperts = 1024;
 
