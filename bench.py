@@ -127,10 +127,20 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_hash() -> str:
+def code_only(text: str) -> str:
+    """C++ source without its comments and whitespace: edits to comments alone
+    leave the compiled kernel, and so this text, unchanged."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return re.sub(r"\s+", "", text)
+
+
+def kernel_hash(read=None) -> str:
+    """Hash of the combine kernel's code (comments and whitespace ignored)."""
+    read = read or (lambda f: open(os.path.join(ROOT, f)).read())
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, f), "rb").read())
+        h.update(code_only(read(f)).encode())
     return h.hexdigest()[:16]
 
 

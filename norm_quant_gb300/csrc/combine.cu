@@ -24,14 +24,17 @@
 //   * persistent CTAs, one per SM by default; token t goes to CTA t mod grid;
 //   * one producer warp walks the CTA's tokens.  A token needs its valid
 //     expert rows in ascending j, then the shared row, then the residual row;
-//     the producer packs up to R of them into one slot of a shared-memory
-//     ring (one cp.async.bulk per 2H-byte row, all completing on the slot's
-//     "full" mbarrier) and writes the slot's weights and flags beside it;
+//     they are spread evenly over as few slots of a shared-memory ring as the
+//     slot capacity R (up to 12 rows) allows.  Lane q of the producer stages
+//     row q of a slot: one cp.async.bulk of the 2H-byte row, completing on the
+//     slot's "full" mbarrier, and the row's weight beside the slot; lane 0
+//     then publishes the slot's count and flags and arms the barrier.
 //     row_map / weights of the next token are prefetched meanwhile;
 //   * consumer warps own 8-element vectors v = slot * NC + thread of the row;
-//     per ring slot they wait once, load all R rows' vectors (R * VPT
-//     independent 16-byte shared loads), accumulate fp32 in registers in
-//     row order, and release the slot on its "empty" mbarrier;
+//     per ring slot they wait once, then take its rows in register chunks
+//     (all of a chunk's 16-byte shared loads, with its weights in one vector
+//     load, before its sums), accumulate fp32 in row order, and release the
+//     slot on its "empty" mbarrier;
 //   * after a token's last slot: bf16 stores, a sum of squares reduced by
 //     warp shuffles and an mbarrier-synchronised cross-warp sum, the norm,
 //     and the block quantiser (an MXFP8 block is 4 consecutive lanes, NVFP4 2);

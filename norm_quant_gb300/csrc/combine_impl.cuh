@@ -745,10 +745,11 @@ inline int choose_split(int32_t H, int64_t, int32_t quant, int forced)
 // warps x 4 (latency-bound) and 80 % for 28 warps x 1 (per-row overhead); at
 // H = 4096, 16 warps x 1 beat 8 x 2.  Rows per ring slot: the fewest slots
 // per token that leave room for three slots (measured, Gemma NVFP4 at
-// H = 4096, 9 rows a token: 5 rows a slot 0.84 of copy bandwidth, 3 rows 0.77,
-// 8 rows with only two slots 0.79; prefill at H = 7168, 10 rows: 4 rows 0.98,
-// 5 rows with two slots 0.96).  Ring: about kDefaultRingBytes of rows, at
-// least 3 slots where they fit, within the shared-memory budget.
+// H = 4096, 9 rows a token: one slot of 9 rows 0.93 of copy bandwidth, two of
+// 5 + 4 rows 0.85, three of 3 rows 0.78, 8-row slots with only two in the
+// ring 0.79; prefill at H = 7168, 10 rows: two slots of 5 rows 0.99).  Ring:
+// about kDefaultRingBytes of rows, at least 3 slots where they fit, within
+// the shared-memory budget.
 // Split rows (when requested): one vector per thread over the H / split
 // columns, and a ring that holds a whole token, so that the producer never
 // waits inside a token and several CTAs fit on one SM.
