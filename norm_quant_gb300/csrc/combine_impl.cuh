@@ -63,14 +63,15 @@ struct Params {
 };
 
 struct SmemLayout {
-    uint32_t row_stride, slot_stride, bars, meta, red, gamma, total;
+    uint32_t row_stride, slot_stride, bars, meta, red, gamma, rtab, total;
 };
 
 // Shared memory of one CTA handling Hl columns of each row: the ring, its
 // barriers (full[S], empty[S], the cross-warp reduction barrier, the gamma
 // copy's barrier, and the two cross-CTA reduction barriers of a split
 // token), the slots' StageMeta, two buffers of per-warp partial sums for
-// csize CTAs, then (with a norm) the Hl gamma values.
+// csize CTAs, then (with a norm) the Hl gamma values, then a table of the
+// reciprocals of the e4m3 block scales (NVFP4).
 __host__ __device__ inline SmemLayout smem_layout(int32_t Hl, int32_t stages, int32_t rows, int32_t ncw,
                                                   int32_t csize, bool with_gamma)
 {
@@ -81,7 +82,8 @@ __host__ __device__ inline SmemLayout smem_layout(int32_t Hl, int32_t stages, in
     L.meta = L.bars + (2u * stages + 4u) * 8u;
     L.red = L.meta + static_cast<uint32_t>(stages) * static_cast<uint32_t>(sizeof(StageMeta));
     L.gamma = (L.red + 2u * static_cast<uint32_t>(csize) * static_cast<uint32_t>(ncw) * 4u + 127u) & ~127u;
-    L.total = L.gamma + (with_gamma ? static_cast<uint32_t>(Hl) * 2u : 0u);
+    L.rtab = (L.gamma + (with_gamma ? static_cast<uint32_t>(Hl) * 2u : 0u) + 15u) & ~15u;
+    L.total = L.rtab + 128u * 4u;  // the reciprocals of the 128 non-negative e4m3 codes
     return L;
 }
 
@@ -260,6 +262,13 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
             mbar_init(xbar0 + 8u, csize * ncw);
         }
         fence_mbar_init();
+    }
+    if constexpr (QUANT == MOE_QUANT_NVFP4) {
+        // the correctly rounded fp32 reciprocal of every non-negative e4m3
+        // code's value (0 for code 0, which is never divided by)
+        float *rtab = reinterpret_cast<float *>(smem + L.rtab);
+        for (uint32_t c = threadIdx.x; c < 128u; c += blockDim.x)
+            rtab[c] = c ? __frcp_rn(e4m3_code_value(c)) : 0.f;
     }
     // with SPLIT, every CTA's barriers are initialised before any peer arrives on them
     if constexpr (SPLIT)
@@ -667,13 +676,12 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                         amax = vv ? amax : 0.f;
                         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
                         const uint32_t sc = cvt_e4m3x2(__fdiv_rn(amax, 6.0f), 0.f) & 0xFFu;
-                        const float sf = e4m3_code_value(sc);
                         if (vv) {
                             uint32_t packed = 0;
-                            if (sf != 0.f) {
+                            if (sc != 0u) {
                                 // elements are scaled by the block scale's correctly
-                                // rounded fp32 reciprocal
-                                const float rs = __frcp_rn(sf);
+                                // rounded fp32 reciprocal, from the table
+                                const float rs = reinterpret_cast<const float *>(smem + L.rtab)[sc];
                                 float qv[8];
 #pragma unroll
                                 for (int i = 0; i < 8; ++i)
