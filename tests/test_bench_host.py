@@ -1,0 +1,52 @@
+"""The bench's host-side arithmetic, on the CPU: the algorithmic byte counts
+behind every roofline fraction, checked against the per-workload totals
+derived independently in the survey's measurement table (reads of the k
+expert rows, the shared and residual rows, row_map and weights, gamma, and
+the written outputs and scales), and the code-only source hash that decides
+whether a recorded ncu traffic figure still applies."""
+import pytest
+
+import bench
+
+
+@pytest.mark.parametrize("name,n_valid,total_mb", [
+    # prefill: 469.76 MB rows + 117.44 shared/residual + 0.28 metadata + 89.00 writes
+    ("prefill", 4096 * 8, 676.48),
+    # Gemma NVFP4: 536.87 + 67.11 + 0.53 + 85.98
+    ("gemma", 8192 * 8, 690.49),
+    # decode: 7.34 + 0.92 + 0.02 + 1.84
+    ("decode", 64 * 8, 10.11),
+])
+def test_algorithmic_bytes_match_the_workload_table(name, n_valid, total_mb):
+    wl = bench.workload(name)
+    b = bench.algorithmic_bytes(wl, n_valid)
+    assert b["total"] == b["rows"] + b["other_reads"] + b["meta"] + b["writes"]
+    assert abs(b["total"] / 1e6 - total_mb) < 0.01
+
+
+def test_byte_count_follows_dtypes_and_formats():
+    base = bench.algorithmic_bytes(bench.workload("prefill"), 32768)
+    fp16 = bench.algorithmic_bytes(bench.workload("fp16"), 32768)
+    mxfp4 = bench.algorithmic_bytes(bench.workload("mxfp4"), 32768)
+    T, H, k = 4096, 7168, 8
+    assert base["meta"] - fp16["meta"] == 2 * k * T          # 2-byte router weights
+    assert base["writes"] - mxfp4["writes"] == H // 2 * T    # 4-bit codes, same scale bytes
+    assert base["rows"] == fp16["rows"] == mxfp4["rows"] == 32768 * 2 * H
+
+
+def test_code_only_ignores_comments_and_whitespace():
+    a = "int f(int x) { // add one\n  return x + 1; /* block\n comment */ }\n"
+    b = "int f(int x)\n{\n    return x + 1;\n}"
+    c = "int f(int x) { return x + 2; }"
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only(a) != bench.code_only(c)
+
+
+def test_kernel_hash_changes_with_code_not_with_comments():
+    src = {f: open(f"{bench.ROOT}/{f}").read() for f in bench.KERNEL_SOURCES}
+    h0 = bench.kernel_hash(lambda f: src[f])
+    first = bench.KERNEL_SOURCES[0]
+    commented = dict(src, **{first: "// a new comment line\n" + src[first]})
+    assert bench.kernel_hash(lambda f: commented[f]) == h0
+    edited = dict(src, **{first: src[first] + "\nstatic int extra_symbol = 1;\n"})
+    assert bench.kernel_hash(lambda f: edited[f]) != h0
