@@ -1,9 +1,10 @@
 """The bench's host-side arithmetic, on the CPU: the algorithmic byte counts
-behind every roofline fraction, checked against the per-workload totals
-derived independently in the survey's measurement table (reads of the k
-expert rows, the shared and residual rows, row_map and weights, gamma, and
-the written outputs and scales), and the code-only source hash that decides
-whether a recorded ncu traffic figure still applies."""
+behind every roofline fraction, checked against per-workload totals worked
+out by hand from the byte formula (reads of the k expert rows at 2H bytes,
+the shared and residual rows, 8k bytes of row_map and weights per token and
+gamma once; writes of each 16-bit output, the fp8 / fp4 codes and the scale
+bytes), and the code-only source hash that decides whether a recorded ncu
+traffic figure still applies."""
 import pytest
 
 import bench
