@@ -69,7 +69,7 @@ typedef struct CUstream_st *moe_stream_t;
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,    /* null / misaligned pointer, bad size or enum */
-    MOE_ERR_UNSUPPORTED = 2,    /* valid request outside this build's limits */
+    MOE_ERR_UNSUPPORTED = 2,    /* valid request outside this library's limits */
     MOE_ERR_WORKSPACE = 3,      /* workspace missing or too small */
     MOE_ERR_INVALID_EXPERT = 4, /* a topk id outside [-1, E) (device-detected) */
     MOE_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed */

@@ -38,7 +38,7 @@ extern "C" const char *moe_status_string(int status)
     switch (status) {
     case MOE_OK: return "MOE_OK";
     case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
-    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: outside this build's limits";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: outside this library's limits";
     case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing or too small";
     case MOE_ERR_INVALID_EXPERT: return "MOE_ERR_INVALID_EXPERT: a topk id outside [-1, E)";
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";

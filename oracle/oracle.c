@@ -34,7 +34,7 @@
  *    output_scalar_scale (per-tensor global scale applied before FP4 block
  *    scaling), sf_layout (linear default, or swizzled).
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent (the plainest one the rest supports):
  *  R1 rows of one expert are stored in ascending (token, slot) order;
  *  R2 ids outside [-1, E) are treated as padding and reported;
  *  R4 router weights are used as given (no renormalisation); a padded slot

@@ -2,7 +2,8 @@
 the GPU and through the oracle on the CPU, and compare with the stated
 tolerances.
 
-Tolerances (from the task's correctness bar, derived in the design doc):
+Tolerances (the accuracy bar for this path, with the fp32 rounding terms of
+the kernel's sums added):
   * routing (counts, offsets, row_map, src_row): bit-exact;
   * bf16 outputs: |gpu - oracle| <= 2 bf16 ulps of the oracle value plus
     gamma_k * (sum of |terms|), gamma_k = (k + 3) * 2^-24 the fp32 forward
