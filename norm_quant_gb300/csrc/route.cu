@@ -21,11 +21,14 @@
 // counts its chunk into its own column of an expert-major shared histogram;
 // each slot's rank inside its chunk comes from warp ballots over the bits of
 // the expert ids (no atomics); one warp per 8 experts turns the columns into
-// prefixes with shuffle scans; after a cluster barrier every CTA reads the
-// other CTAs' per-expert totals through distributed shared memory, a second
-// barrier ends all remote access, and each CTA derives counts, offsets and
-// its bases locally and scatters.  Cluster barriers are
-// hardware barriers over co-scheduled CTAs, so nothing spins.
+// prefixes with shuffle scans and stores each per-expert total straight into
+// every CTA's shared memory (distributed shared memory; a cluster barrier
+// split around the first phase guarantees every CTA has started); one more
+// cluster barrier makes the totals visible, and each CTA derives counts,
+// offsets and its bases locally and scatters.  Batches of up to
+// kSmallMaxSlots slots use one CTA of 8 warps instead (route_small_kernel).
+// Cluster barriers are hardware barriers over co-scheduled CTAs, so nothing
+// spins.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -260,7 +263,9 @@ struct FusedPlan {
 size_t fused_smem(int32_t E)
 {
     // hist[E][33] + all_tot[16][E] + base[E] + off[E + 1] + wsum[32] + the CTA's error flag
-    return (static_cast<size_t>(kHistPitch + kFusedMaxCtas + 2) * E + 1 + 32 + 1) * sizeof(int32_t);
+    // + the CTAs' flags (CTA 0)
+    return (static_cast<size_t>(kHistPitch + kFusedMaxCtas + 2) * E + 1 + 32 + 1 + kFusedMaxCtas) *
+           sizeof(int32_t);
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -275,15 +280,32 @@ __device__ __forceinline__ void cluster_sync_all()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Reads the int32 at the same shared-memory offset as `local` in CTA `rank`
-// of this cluster.
-__device__ __forceinline__ int32_t ld_dsmem(const int32_t *local, uint32_t rank)
+// Stores v at the same shared-memory offset as `local` in CTA `rank`.
+__device__ __forceinline__ void st_dsmem(int32_t *local, uint32_t rank, int32_t v)
 {
-    uint32_t remote, v;
+    uint32_t remote;
     asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
-    return static_cast<int32_t>(v);
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
 }
+
+// Stores four int32 (16-byte aligned `local`) at the same offset in CTA `rank`.
+__device__ __forceinline__ void st_dsmem_v4(int32_t *local, uint32_t rank, int32_t a, int32_t b, int32_t c,
+                                            int32_t d)
+{
+    uint32_t remote;
+    asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// The two halves of a cluster barrier, for a thread that has work to do in
+// between (arrive without ordering; wait with acquire).
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
 // One cluster of gridDim.x CTAs (the whole grid), 32 warps each; warp w of
 // CTA b owns the chunk of PL * 32 consecutive slots starting at
@@ -302,12 +324,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     int32_t *off = base + E;                                          // [E + 1]
     int32_t *wsum = off + E + 1;                                      // [32]
     int32_t &cta_bad = wsum[32];                                      // an id outside [-1, E) seen here
+    int32_t *flags = wsum + 33;                                       // [16]: each CTA's cta_bad (CTA 0)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const int nctas = static_cast<int>(gridDim.x);
     const int64_t first = (static_cast<int64_t>(rank) * kFusedWarps + warp) * (PL * 32);
     const uint32_t lt = (1u << lane) - 1u;
     allow_dependent_launch();  // the combine may start its setup now
+    // the CTAs push their totals into one another's shared memory later; a
+    // cluster barrier split around phase 1 makes sure every CTA has started
+    if (nctas > 1)
+        cluster_arrive_relaxed();
 
     // 1. each warp counts its chunk into its own column of hist and ranks
     //    every slot among the earlier slots of the chunk with the same expert.
@@ -350,8 +377,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     // release wait for the store to reach L2)
     {
         const int32_t b = __syncthreads_or(bad ? 1 : 0);
-        if (threadIdx.x == 0)
+        if (nctas > 1)
+            cluster_wait();
+        if (threadIdx.x == 0) {
             cta_bad = b;
+            if (nctas > 1)
+                st_dsmem(&flags[rank], 0, b);
+            else
+                flags[0] = b;
+        }
     }
     // 2. per expert: exclusive prefix over the 32 warp columns (a shuffle
     //    scan, kScanIlp experts at a time per warp) and the CTA's total
@@ -370,44 +404,46 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                 if (lane >= d)
                     incl[q] += o;
             }
+        int32_t tot[kScanIlp];
 #pragma unroll
         for (int q = 0; q < kScanIlp; ++q) {
             const int e = e0 + q;
-            if (e < E) {
+            tot[q] = __shfl_sync(0xffffffffu, incl[q], 31);
+            if (e < E)
                 hist[e * kHistPitch + lane] = incl[q] - x[q];
-                if (lane == 31)
-                    all_tot[rank * E + e] = incl[q];  // this CTA's total, in its own row
+        }
+        // this CTA's totals go into row `rank` of every CTA's all_tot: lane
+        // b stores them in CTA b, 16 bytes at a time where E allows
+        if (nctas == 1) {
+            if (lane == 0) {
+#pragma unroll
+                for (int q = 0; q < kScanIlp; ++q)
+                    if (e0 + q < E)
+                        all_tot[e0 + q] = tot[q];
+            }
+        } else if (lane < nctas) {
+            int32_t *row = &all_tot[rank * E + e0];
+            if (E % kScanIlp == 0) {
+                st_dsmem_v4(row, static_cast<uint32_t>(lane), tot[0], tot[1], tot[2], tot[3]);
+                st_dsmem_v4(row + 4, static_cast<uint32_t>(lane), tot[4], tot[5], tot[6], tot[7]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < kScanIlp; ++q)
+                    if (e0 + q < E)
+                        st_dsmem(row + q, static_cast<uint32_t>(lane), tot[q]);
             }
         }
     }
-    // 3. publish the totals; every CTA pulls the other CTAs' rows (all loads
-    //    in flight at once); the second barrier keeps every CTA alive until
-    //    no one reads its shared memory any more.  A lone CTA needs only its
-    //    own barrier.
+    // 3. one barrier makes every CTA's pushed totals and flags visible; no
+    //    CTA touches another's shared memory after it.  A lone CTA needs only
+    //    its own barrier.
     if (nctas > 1)
         cluster_sync_all();
     else
         __syncthreads();
-    // CTA 0's first warp reads the CTAs' flags at once, lane b from CTA b
     int32_t any_bad = 0;
-    if (rank == 0 && warp == 0) {
-        const int32_t f = lane >= nctas ? 0 : (lane == 0 ? cta_bad : ld_dsmem(&cta_bad, static_cast<uint32_t>(lane)));
-        any_bad = __any_sync(0xffffffffu, f != 0) ? 1 : 0;
-    }
-    for (int e = threadIdx.x; e < E; e += kFusedThreads) {
-        int32_t x[kFusedMaxCtas];
-#pragma unroll
-        for (int b = 0; b < kFusedMaxCtas; ++b)
-            x[b] = (b < nctas && b != static_cast<int>(rank)) ? ld_dsmem(&all_tot[b * E + e], static_cast<uint32_t>(b)) : 0;
-#pragma unroll
-        for (int b = 0; b < kFusedMaxCtas; ++b)
-            if (b < nctas && b != static_cast<int>(rank))
-                all_tot[b * E + e] = x[b];
-    }
-    if (nctas > 1)
-        cluster_sync_all();
-    else
-        __syncthreads();
+    if (rank == 0 && warp == 0)
+        any_bad = __any_sync(0xffffffffu, lane < nctas && flags[lane] != 0) ? 1 : 0;
     if (rank == 0 && threadIdx.x == 0)
         *err = any_bad;
     // 4. counts, exclusive scan over experts, this CTA's base per expert
