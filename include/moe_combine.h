@@ -275,8 +275,8 @@ moe_status moe_combine(const moe_combine_args *args, moe_stream_t stream);
  * (performance only: every plan computes identical results).  Each argument
  * 0 restores the automatic choice:
  *   vpt            8-element vectors per consumer thread: 1, 2, 4 or 8
- *                  (ignored where it cannot cover H; at most 28, 16, 8, 8
- *                  consumer warps respectively);
+ *                  (ignored where it cannot cover H; at most 16, 16, 8, 8
+ *                  consumer warps respectively, so 1 covers H <= 4096);
  *   rows_per_slot  most rows staged per ring slot, 1..12 (a token's rows are
  *                  spread evenly over as few slots as that allows; fewer
  *                  where two slots would not fit in shared memory);
