@@ -75,6 +75,7 @@ SYMBOLS = {
     "moe_scales_bytes": (C.c_int, [C.c_int64, C.c_int32, C.c_int32, C.c_int32,
                                    C.POINTER(C.c_size_t)]),
     "moe_tuning_set": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
+    "moe_debug_stall": (C.c_int, [C.c_int64]),
     "moe_dispatch_permute": (C.c_int, [C.c_void_p, C.c_int64, C.c_int32, C.c_void_p, C.c_int32,
                                        C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p]),
 }
@@ -193,6 +194,13 @@ def moe_tuning_set(vpt: int = 0, rows_per_slot: int = 0, ring_kib: int = 0, ctas
     """Overrides the launch plans (0 = automatic); results do not depend on it."""
     _check(lib().moe_tuning_set(vpt, rows_per_slot, ring_kib, ctas_per_sm, route_cluster, combine_split),
            "moe_tuning_set")
+
+
+def moe_debug_stall(slots: int = -1) -> None:
+    """Test hook: the combine's CTA 0 stops staging rows after `slots` ring
+    slots, so its bounded waits run out and the status reports a timeout
+    (-1 turns it off)."""
+    _check(lib().moe_debug_stall(slots), "moe_debug_stall")
 
 
 def combine_args(*, expert_out, row_map, router_weights, shared_out=None, residual=None,

@@ -92,6 +92,14 @@ extern "C" moe_status moe_tuning_set(int32_t vpt, int32_t rows_per_slot, int32_t
     return MOE_OK;
 }
 
+extern "C" moe_status moe_debug_stall(int64_t slots)
+{
+    if (slots < -1)
+        return MOE_ERR_INVALID_ARG;
+    g_tuning.stall_after = slots;
+    return MOE_OK;
+}
+
 extern "C" moe_status moe_combine(const moe_combine_args *a, moe_stream_t stream)
 {
     if (!a)
@@ -179,6 +187,7 @@ extern "C" moe_status moe_combine(const moe_combine_args *a, moe_stream_t stream
         p.rows = pl.rows;
         p.split = pl.split;
         p.hl = pl.hl;
+        p.stall_after = g_tuning.stall_after;
         return a->io_dtype == MOE_IO_FP16 ? launch_io<1>(p, pl, a->quant, s) : launch_io<0>(p, pl, a->quant, s);
     };
     // rows a token may need: its valid expert rows, the shared row, the residual row

@@ -59,6 +59,7 @@ struct Params {
     int32_t slot_major;    // expert_out is [k, T, H]: row of (t, j) is j * T + t
     int32_t split;         // CTAs sharing one token (the cluster size), 1 = a whole row per CTA
     int32_t hl;            // columns each CTA handles: H / split
+    int64_t stall_after;   // test hook (moe_debug_stall): -1 off, else CTA 0 stages this many slots
     int64_t sf_cols, sf_cols_pad, sf_rows_pad;
 };
 
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
             int stage = 0;
             uint32_t phase = 0;
             int64_t issued = 0;
-            bool ok = true;
+            bool ok = true, stalled = false;
             int64_t t = unit0;
             int32_t r_next = -1;
             float w_next = 0.f;
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                 r_next = row_of(t);
                 w_next = load_weight(p.weights, t * k + lane, p.weight_dtype);
             }
-            for (; t < p.T && ok; t += nunits()) {
+            for (; t < p.T && ok && !stalled; t += nunits()) {
                 const int32_t r = r_next;
                 const float w = w_next;
                 const int64_t tn = t + nunits();
@@ -323,6 +324,12 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                 const int nslots = n > 0 ? (n + R - 1) / R : 1;
                 int i = 0, si = 0;
                 do {
+                    if (p.stall_after >= 0 && blockIdx.x == 0 && issued >= p.stall_after) {
+                        // test hook: CTA 0 stages nothing more, so that its
+                        // consumers' bounded waits run out
+                        stalled = true;
+                        break;
+                    }
                     const int left = nslots - si;
                     const int ns = (n - i + left - 1) / left;
                     // lane q stages row i + q: the (i + q)-th valid expert slot in
@@ -714,6 +721,7 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
 // Process-wide plan overrides set by moe_tuning_set (0 = automatic).
 struct Tuning {
     int vpt = 0, rows = 0, ring_kib = 0, ctas_per_sm = 0, split = 0;
+    int64_t stall_after = -1;  // moe_debug_stall
 };
 extern Tuning g_tuning;
 

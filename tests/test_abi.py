@@ -103,6 +103,8 @@ def test_tuning_validation(L):
         assert L.moe_tuning_set(0, 0, 0, 0, 0, bad) == 1
     assert L.moe_tuning_set(2, 2, 144, 1, -1, 8) == 0
     assert L.moe_tuning_set(0, 0, 0, 0, 0, 0) == 0
+    assert L.moe_debug_stall(-2) == 1
+    assert L.moe_debug_stall(-1) == 0
 
 
 def test_combine_null_args(L):

@@ -226,6 +226,24 @@ def test_row_out_of_range_is_reported_and_skipped():
                       "skipped slot")
 
 
+def test_bounded_wait_timeout_is_reported_and_the_context_survives():
+    """A wait that runs out (CTA 0's producer stops staging rows through the
+    test hook) is reported as MOE_ERR_DEVICE_TIMEOUT after the 2 s limit,
+    without a fault; the next call on the same context is fully correct."""
+    wl = _wl(T=300, H=7168, k=8, E=256, shared_std=0.5, quant="mxfp8", outputs=("residual", "quant"))
+    inp = synth.make_inputs(wl)
+    d_rm, orm = route_and_check(inp["topk_ids"], wl.E)
+    try:
+        nqg.moe_debug_stall(1)
+        got = gpu_combine(wl, inp, d_rm)
+    finally:
+        nqg.moe_debug_stall(-1)
+    assert got["status"] == nqg.MOE_ERR_DEVICE_TIMEOUT
+    again = gpu_combine(wl, inp, d_rm, canary=True)
+    assert again["status"] == 0
+    compare(wl, inp, orm, again)
+
+
 def test_repeat_runs_identical_and_side_stream():
     wl = dataclasses.replace(synth.PREFILL, T=700, name="repeat")
     inp = synth.make_inputs(wl)
