@@ -298,10 +298,11 @@ moe_status moe_combine(const moe_combine_args *args, moe_stream_t stream);
 moe_status moe_tuning_set(int32_t vpt, int32_t rows_per_slot, int32_t ring_kib, int32_t ctas_per_sm,
                           int32_t route_cluster, int32_t combine_split);
 
-/* Test hook for the combine's failure detection, for the rest of the process:
- * with slots >= 0, the combine's CTA 0 stops staging rows after that many
- * ring slots, so that its consumers' bounded waits run out (about 2 s) and
- * the call records MOE_ERR_DEVICE_TIMEOUT in its status word; the other CTAs
+/* Test hook for failure detection, for the rest of the process: with
+ * slots >= 0, CTA 0 of the combine stops staging rows after that many ring
+ * slots, and CTA 0 of the dispatch permute stops loading token rows after
+ * that many tokens, so that their bounded waits run out (about 2 s) and the
+ * call records MOE_ERR_DEVICE_TIMEOUT in its status word; the other CTAs
  * finish normally.  Nothing faults, and the CUDA context stays usable.
  * -1 (the default) turns it off.  Returns MOE_OK or MOE_ERR_INVALID_ARG.
  * (No counterpart on the pages.) */

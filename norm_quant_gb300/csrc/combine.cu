@@ -92,6 +92,8 @@ extern "C" moe_status moe_tuning_set(int32_t vpt, int32_t rows_per_slot, int32_t
     return MOE_OK;
 }
 
+int64_t nqg::debug_stall_slots() { return g_tuning.stall_after; }
+
 extern "C" moe_status moe_debug_stall(int64_t slots)
 {
     if (slots < -1)

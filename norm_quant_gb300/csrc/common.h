@@ -17,6 +17,10 @@ int sm_count();
 // three-kernel path, 1..16 the largest cluster the single-launch path may use.
 void set_route_cluster(int v);
 
+// moe_debug_stall's setting: -1, or the ring slots (combine) / token loads
+// (dispatch permute) that CTA 0 issues before it stops.
+int64_t debug_stall_slots();
+
 // Status of the launches just made: MOE_ERR_CUDA if any failed.
 inline moe_status launch_status()
 {

@@ -32,7 +32,7 @@ __device__ __forceinline__ void report(int32_t *status, int32_t code)
 __global__ void __launch_bounds__(32) dispatch_kernel(const uint8_t *__restrict__ x, int64_t T, int32_t H,
                                                       const int32_t *__restrict__ row_map, int32_t k,
                                                       uint8_t *__restrict__ xg, int64_t n_rows,
-                                                      int32_t *__restrict__ status, int32_t S)
+                                                      int32_t *__restrict__ status, int32_t S, int64_t stall_after)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x;
@@ -50,16 +50,21 @@ __global__ void __launch_bounds__(32) dispatch_kernel(const uint8_t *__restrict_
     __syncwarp();
     grid_dependency_wait();  // see the combine kernel: programmatic dependent launch
 
-    auto load = [&](int64_t i) {  // lane 0 only
+    // test hook (moe_debug_stall): CTA 0 issues no loads from token stall_after on
+    const bool stalls = stall_after >= 0 && blockIdx.x == 0;
+    auto load = [&](int64_t i) {  // lane 0 only; false if the hook held it back
+        if (stalls && i >= stall_after)
+            return false;
         const uint32_t s = static_cast<uint32_t>(i % S);
         mbar_arrive_expect_tx(full0 + 8u * s, row_bytes);
         bulk_g2s(ring + s * row_stride, x + (blockIdx.x + i * G) * row_bytes, row_bytes, full0 + 8u * s);
+        return true;
     };
     const int64_t pro = n < S ? n : S;
+    int64_t loaded = 0;  // loads issued (lane 0's count)
     if (lane == 0)
         for (int64_t q = 0; q < pro; ++q)
-            load(q);
-    int64_t loaded = pro;
+            loaded += load(q) ? 1 : 0;
 
     int32_t r_next = (n > 0 && lane < k) ? __ldg(row_map + static_cast<int64_t>(blockIdx.x) * k + lane) : -1;
     bool ok = true;
@@ -98,8 +103,8 @@ __global__ void __launch_bounds__(32) dispatch_kernel(const uint8_t *__restrict_
             // refill the previous token's slot once its stores have read it
             if (i >= 1 && loaded < n) {
                 bulk_wait_read_all_but_one();
-                load(loaded);
-                ++loaded;
+                if (load(loaded))
+                    ++loaded;
             }
         }
     }
@@ -166,7 +171,7 @@ extern "C" moe_status moe_dispatch_permute(const void *x, int64_t T, int32_t H, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, dispatch_kernel, static_cast<const uint8_t *>(x), T, H, row_map, top_k,
-                           static_cast<uint8_t *>(x_grouped), n_rows, status, S) != cudaSuccess) {
+                           static_cast<uint8_t *>(x_grouped), n_rows, status, S, debug_stall_slots()) != cudaSuccess) {
         cudaGetLastError();
         return MOE_ERR_CUDA;
     }

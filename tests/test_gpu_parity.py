@@ -314,6 +314,32 @@ def test_dispatch_permute_parity(T, H, k, E):
     assert np.array_equal(h(xg, np.uint16), want)
 
 
+def test_dispatch_bounded_wait_timeout_is_reported():
+    """The permute's bounded wait runs out when CTA 0 issues no more row
+    loads (test hook): MOE_ERR_DEVICE_TIMEOUT, no fault, and the next call on
+    the same context is exact."""
+    T, H, k, E = 500, 1024, 8, 64
+    rng = np.random.Generator(np.random.PCG64(12))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    d_rm, orm = route_and_check(ids, E)
+    x = synth.bf16_normal(rng, (T, H))
+    xg = torch.zeros((T * k, H), dtype=torch.int16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    try:
+        nqg.moe_debug_stall(0)  # CTA 0 owns one token here (one CTA per token): load none
+        nqg.moe_dispatch_permute(d(x), d_rm, xg, status=status)
+        torch.cuda.synchronize()
+    finally:
+        nqg.moe_debug_stall(-1)
+    assert int(status.item()) == nqg.MOE_ERR_DEVICE_TIMEOUT
+    status.zero_()
+    nqg.moe_dispatch_permute(d(x), d_rm, xg, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    st, want = oracle.dispatch_permute(x, orm, T * k)
+    assert np.array_equal(h(xg, np.uint16), want)
+
+
 def test_dispatch_permute_reports_out_of_range_rows():
     T, H, k = 8, 64, 2
     x = synth.bf16_normal(np.random.Generator(np.random.PCG64(3)), (T, H))
