@@ -839,20 +839,17 @@ template <int VPT, int QUANT, int IO, bool SPLIT>
 moe_status launch_t(const Params &p, const Plan &pl, cudaStream_t stream)
 {
     auto kern = combine_kernel<VPT, QUANT, IO, SPLIT>;
-    static int configured_for[64] = {0};  // per device: dynamic smem already allowed
+    static SmemLimit smem_limit;  // per instantiation
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return MOE_ERR_CUDA;
     const int need = static_cast<int>(pl.smem.total);
     if (need > 227 * 1024)
         return MOE_ERR_UNSUPPORTED;
-    if (dev < 0 || dev >= 64 || configured_for[dev] < need) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, need) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        if (SPLIT && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        if (dev >= 0 && dev < 64)
-            configured_for[dev] = need;
+    if (ensure_dynamic_smem(kern, dev, need, smem_limit) != cudaSuccess ||
+        (SPLIT && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -872,6 +869,8 @@ moe_status launch_t(const Params &p, const Plan &pl, cudaStream_t stream)
         // caller then falls back to whole rows); the answer is kept per
         // device, cluster size and shared-memory size
         static int fits_split[64][5], fits_smem[64][5];
+        static std::mutex fits_mu;
+        std::lock_guard<std::mutex> guard(fits_mu);
         int li = 0;
         while ((2 << li) < pl.split)
             ++li;

@@ -144,16 +144,13 @@ extern "C" moe_status moe_dispatch_permute(const void *x, int64_t T, int32_t H, 
     int S = static_cast<int>(kDispatchCtaSmem / (row_stride + 8));
     S = S < 2 ? 2 : (S > kDispatchMaxSlots ? kDispatchMaxSlots : S);
     const size_t smem = static_cast<size_t>(S) * (row_stride + 8);
-    static int configured_for[64] = {0};
+    static SmemLimit smem_limit;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (dev < 0 || dev >= 64 || configured_for[dev] < static_cast<int>(smem)) {
-        if (cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        if (dev >= 0 && dev < 64)
-            configured_for[dev] = static_cast<int>(smem);
+    if (ensure_dynamic_smem(dispatch_kernel, dev, static_cast<int>(smem), smem_limit) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
     }
     const int per_sm = static_cast<int>((220 * 1024) / (smem + 1024));
     const int64_t ctas = static_cast<int64_t>(sm_count()) * (per_sm < 1 ? 1 : per_sm);

@@ -1,5 +1,6 @@
 // noalloc.cu -- the routing build for callers that cannot allocate device
 // memory: its scratch lives in a fixed array that the library itself holds.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -17,19 +18,19 @@ static __device__ __align__(256) unsigned char g_route_scratch[MOE_NOALLOC_SCRAT
 // device (with that device current); nullptr if the lookup fails.
 void *route_scratch_address()
 {
-    static void *addr[64];
+    static std::atomic<void *> addr[64];  // static storage: starts null
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return nullptr;
-    if (!addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess) {
+    void *a = addr[dev].load(std::memory_order_acquire);
+    if (!a) {
+        if (cudaGetSymbolAddress(&a, g_route_scratch) != cudaSuccess) {
             cudaGetLastError();
             return nullptr;
         }
-        addr[dev] = p;
+        addr[dev].store(a, std::memory_order_release);  // every thread finds the same address
     }
-    return addr[dev];
+    return a;
 }
 
 } // namespace

@@ -693,8 +693,11 @@ FusedFn fused_fn(int per_lane)
 // device; cached per device, kernel, cluster size and 32 KiB smem bucket.
 bool fused_fits(FusedFn fn, int per_lane, int ctas, size_t smem)
 {
-    static signed char cache[64][6][kFusedMaxCtas + 1][8];  // 0 unknown, 1 yes, -1 no
-    static bool attr_set[64][6];
+    // answers and attribute state, shared by host threads (static storage:
+    // they start at zero)
+    static std::atomic<signed char> cache[64][6][kFusedMaxCtas + 1][8];  // 0 unknown, 1 yes, -1 no
+    static std::atomic<bool> attr_set[64][6];
+    static std::mutex attr_mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return false;
@@ -702,16 +705,20 @@ bool fused_fits(FusedFn fn, int per_lane, int ctas, size_t smem)
     const int bucket = static_cast<int>((smem + 32 * 1024 - 1) / (32 * 1024));
     if (bucket >= 8 || static_cast<size_t>(bucket) * 32 * 1024 > 227 * 1024)
         return false;
-    signed char &c = cache[dev][pl_idx][ctas][bucket];
-    if (c)
-        return c > 0;
-    if (!attr_set[dev][pl_idx]) {
-        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess ||
-            cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-            cudaGetLastError();
-            return false;
+    std::atomic<signed char> &c = cache[dev][pl_idx][ctas][bucket];
+    const signed char known = c.load(std::memory_order_acquire);
+    if (known)
+        return known > 0;
+    if (!attr_set[dev][pl_idx].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> guard(attr_mu);
+        if (!attr_set[dev][pl_idx].load(std::memory_order_relaxed)) {
+            if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess ||
+                cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+                cudaGetLastError();
+                return false;
+            }
+            attr_set[dev][pl_idx].store(true, std::memory_order_release);
         }
-        attr_set[dev][pl_idx] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -727,7 +734,7 @@ bool fused_fits(FusedFn fn, int per_lane, int ctas, size_t smem)
     int n = 0;
     const bool ok = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void *>(fn), &cfg) == cudaSuccess && n > 0;
     cudaGetLastError();
-    c = ok ? 1 : -1;
+    c.store(ok ? 1 : -1, std::memory_order_release);
     return ok;
 }
 

@@ -244,6 +244,45 @@ def test_bounded_wait_timeout_is_reported_and_the_context_survives():
     compare(wl, inp, orm, again)
 
 
+def test_concurrent_calls_from_two_host_threads():
+    """Two host threads call the combine at once, on their own streams, with
+    workloads that need different shared-memory sizes (and so different
+    kernel attributes); both match the oracle."""
+    import threading
+    cases = [dataclasses.replace(synth.PREFILL, T=200, name="thread_mxfp8"),
+             dataclasses.replace(synth.GEMMA_NVFP4, T=150, name="thread_nvfp4")]
+    prepared = []
+    for wl in cases:
+        inp = synth.make_inputs(wl)
+        d_rm, orm = route_and_check(inp["topk_ids"], wl.E)
+        g = nvfp4_global_scale(wl, inp, orm) if wl.quant == "nvfp4" else 1.0
+        prepared.append((wl, inp, d_rm, orm, g))
+    results, errors = [None] * len(cases), []
+
+    def run(i):
+        try:
+            wl, inp, d_rm, orm, g = prepared[i]
+            s = torch.cuda.Stream()
+            out = []
+            for _ in range(3):
+                with torch.cuda.stream(s):
+                    out.append(gpu_combine(wl, inp, d_rm, global_scale=g, stream=s))
+            results[i] = out
+        except Exception as e:  # reported below, in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(len(cases))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for (wl, inp, d_rm, orm, g), outs in zip(prepared, results):
+        for got in outs:
+            assert got["status"] == 0
+            compare(wl, inp, orm, got, global_scale=g)
+
+
 def test_repeat_runs_identical_and_side_stream():
     wl = dataclasses.replace(synth.PREFILL, T=700, name="repeat")
     inp = synth.make_inputs(wl)
