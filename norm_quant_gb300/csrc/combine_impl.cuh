@@ -682,7 +682,7 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                         }
                         amax = vv ? amax : 0.f;
                         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                        const uint32_t sc = cvt_e4m3x2(__fdiv_rn(amax, 6.0f), 0.f) & 0xFFu;
+                        const uint32_t sc = cvt_e4m3x2(div6_rn(amax), 0.f) & 0xFFu;
                         if (vv) {
                             uint32_t packed = 0;
                             if (sc != 0u) {

@@ -206,6 +206,24 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ------------------------------------------------------------ arithmetic
+
+// x / 6 rounded to nearest even, without a division, wherever the quotient
+// is a normal float: q = RN(x * RN(1/6)) is within one ulp of x / 6, the
+// remainder x - 6q is exact in one fused multiply-add, and
+// RN(q + (x - 6q) * RN(1/6)) is then the correctly rounded quotient
+// (Markstein's theorem on FMA-corrected division; P. Markstein, IBM J. Res.
+// Dev. 34(1), 1990).  The theorem assumes no underflow: below 2^-126 the
+// result may differ in its last place.  Checked on every finite non-negative
+// float against the correctly rounded division.
+__device__ __forceinline__ float div6_rn(float x)
+{
+    const float c = 0x1.555556p-3f;  // RN(1/6)
+    const float q = __fmul_rn(x, c);
+    const float r = __fmaf_rn(-q, 6.0f, x);
+    return __fmaf_rn(r, c, q);
+}
+
 // ------------------------------------------------------------ conversions
 
 // Two fp32 -> two e4m3 (round to nearest even, saturate to +-448); `lo`
