@@ -80,3 +80,49 @@ def test_random_configuration_matches_the_oracle(i):
     torch.cuda.synchronize()
     assert got["status"] == 0, (wl, layout, plan)
     compare(wl, inp, orm, got, global_scale=g, expert_layout=layout)
+
+
+@pytest.mark.parametrize("i", range(60))
+def test_random_routing_build_matches_the_oracle(i):
+    """Seeded draws of T, top_k, E, padding, invalid ids and routing path
+    (automatic, three kernels, or a cluster cap); counts, offsets, row_map
+    and src_row bit-exact against the oracle."""
+    rng = np.random.Generator(np.random.PCG64(9100 + i))
+    k = int(rng.integers(1, 33))
+    E = int([rng.integers(1, 9), rng.integers(1, 300), rng.integers(1, 8193)][int(rng.integers(3))])
+    T = int([rng.integers(1, 300), rng.integers(1, 5000), rng.integers(1, 500_000 // k + 1)][int(rng.integers(3))])
+    ids = rng.integers(0, E, (T, k)).astype(np.int32)
+    ids[rng.random((T, k)) < rng.choice([0.0, 0.1, 0.5])] = -1
+    if rng.random() < 0.15:
+        ids[rng.random((T, k)) < 0.001] = E + 3  # out of range: reported, treated as padding
+    cluster = int(rng.choice([0, 0, 0, -1, 1, 2, 4, 8, 16]))
+    try:
+        nqg.moe_tuning_set(route_cluster=cluster)
+        route_and_check(ids, E)
+    finally:
+        nqg.moe_tuning_set()
+
+
+@pytest.mark.parametrize("i", range(30))
+def test_random_dispatch_permute_matches_the_oracle(i):
+    """Seeded draws of T, H, top_k and E; the dispatch permute writes every
+    grouped row bit-exactly as the oracle does, and leaves the others."""
+    from _helpers import d, h
+    import oracle
+    rng = np.random.Generator(np.random.PCG64(9300 + i))
+    k = int(rng.integers(1, 17))
+    E = int(rng.integers(k, 400))
+    H = int(8 * rng.integers(1, 16384 // 8 + 1)) if rng.random() < 0.3 else int(8 * rng.integers(1, 1025))
+    T = int(rng.integers(1, max(2, min(3000, 4_000_000 // (H * k)))))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    ids[rng.random((T, k)) < 0.1] = -1
+    d_rm, orm = route_and_check(ids, E)
+    x = synth.bf16_normal(rng, (T, H))
+    n_rows = int((ids >= 0).sum()) + int(rng.integers(0, 4))
+    xg = torch.full((max(n_rows, 1), H), 0x3F80, dtype=torch.int16, device="cuda")[:n_rows]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nqg.moe_dispatch_permute(d(x), d_rm, xg, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    st, want = oracle.dispatch_permute(x, orm, n_rows, fill=0x3F80)
+    assert np.array_equal(h(xg, np.uint16), want)
