@@ -468,26 +468,32 @@ def run_ours(args):
 
     g_step, g_comb = graph_of(step, G), graph_of(combine, G)
 
+    replay_s = []  # device seconds of each replay of the last replay() call
+
     def replay(g, n):
-        """n replays on gs, each after an optional L2 flush; device seconds."""
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        """n replays on gs, each after an optional L2 flush; device seconds.
+        An event after every replay (no synchronisation between them) also
+        gives each replay's duration."""
+        replay_s.clear()
         with torch.cuda.stream(gs):
             if args.l2 == "write":
-                tot = 0.0
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 for _ in range(n):
                     flush.zero_()
                     e0.record(gs)
                     g.replay()
                     e1.record(gs)
                     e1.synchronize()
-                    tot += e0.elapsed_time(e1) / 1e3
-                return tot
-            e0.record(gs)
-            for _ in range(n):
+                    replay_s.append(e0.elapsed_time(e1) / 1e3)
+                return sum(replay_s)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+            ev[0].record(gs)
+            for i in range(n):
                 g.replay()
-            e1.record(gs)
-        e1.synchronize()
-        return e0.elapsed_time(e1) / 1e3
+                ev[i + 1].record(gs)
+        ev[-1].synchronize()
+        replay_s.extend(ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(n))
+        return ev[0].elapsed_time(ev[-1]) / 1e3
 
     replay(g_step, -(-max(3, args.warmup) // G))  # at least W untimed steps
     if world > 1:
@@ -495,6 +501,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         total_s = replay(g_step, K // G)       # timed region: exactly K whole steps
+        step_pct = np.percentile(np.array(replay_s) / G * 1e6, [10, 50, 90])
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
@@ -584,6 +591,8 @@ def run_ours(args):
             "e2e": {"value": job_throughput(world, T, args.e2e_steps, e2e_s), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": (route_kernels + 1) * K,
+            "step_time_us": {"p10": float(step_pct[0]), "p50": float(step_pct[1]), "p90": float(step_pct[2]),
+                             "over": f"{K // G} replays of {G} steps each (rank {rank})"},
             "clocks": clk.summary(),
         }
         if not args.no_cpu_baseline and world == 1 and kind == "prefill":
