@@ -68,8 +68,8 @@ struct SmemLayout {
 };
 
 // Shared memory of one CTA handling Hl columns of each row: the ring, its
-// barriers (full[S], empty[S], the cross-warp reduction barrier, the gamma
-// copy's barrier, and the two cross-CTA reduction barriers of a split
+// barriers (full[S], empty[S], the consumers' abort word, the gamma copy's
+// barrier, and the two cross-CTA reduction barriers of a split
 // token), the slots' StageMeta, two buffers of per-warp partial sums for
 // csize CTAs, then (with a norm) the Hl gamma values, then a table of the
 // reciprocals of the e4m3 block scales (NVFP4).
@@ -245,18 +245,21 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
     const uint32_t col_bytes = static_cast<uint32_t>(col0) * 2u;
     const SmemLayout L = smem_layout(Hl, S, R, ncw, static_cast<int32_t>(csize), p.gamma != nullptr);
     const uint32_t ring = smem_u32(smem);
-    const uint32_t full0 = ring + L.bars, empty0 = full0 + 8u * S, redbar = empty0 + 8u * S;
-    const uint32_t gbar = redbar + 8u;    // the gamma copy
-    const uint32_t xbar0 = redbar + 16u;  // two cross-CTA barriers, by token parity
+    const uint32_t full0 = ring + L.bars, empty0 = full0 + 8u * S;
+    const uint32_t gbar = empty0 + 8u * S + 8u;  // the gamma copy
+    const uint32_t xbar0 = gbar + 8u;            // two cross-CTA barriers, by token parity
     StageMeta *meta = reinterpret_cast<StageMeta *>(smem + L.meta);
     float *red = reinterpret_cast<float *>(smem + L.red);
 
+    // set by a consumer warp whose bounded wait gave up, before it meets the
+    // others at the norm's barrier; read by every consumer warp after it
+    int32_t *abort_word = reinterpret_cast<int32_t *>(smem + L.bars + 16u * S);
     if (threadIdx.x == 0) {
+        *abort_word = 0;
         for (int s = 0; s < S; ++s) {
             mbar_init(full0 + 8u * s, 1);
             mbar_init(empty0 + 8u * s, ncw);
         }
-        mbar_init(redbar, ncw);
         mbar_init(gbar, 1);
         if constexpr (SPLIT) {
             mbar_init(xbar0, csize * ncw);
@@ -415,9 +418,27 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
             }
             const bool do_norm = p.gamma != nullptr;
             const int max_slots = k + 3;  // a token never needs more slots than rows + 1
+            // Without SPLIT, the consumer warps meet at a named hardware barrier
+            // once per token, for the norm.  A warp whose bounded wait gives up
+            // must still meet the others there, or they would wait forever: it
+            // raises abort_word, arrives at the barrier of the token it is in,
+            // and leaves; every warp reads abort_word after that barrier and
+            // leaves before its next store.  A warp reaches a token's barrier
+            // only once that token's slots have all filled, so the barrier the
+            // warp that gave up arrives at is the one every other warp is bound
+            // for.
+            const bool meets = !SPLIT && do_norm;
+            auto give_up = [&]() {
+                if (meets) {
+                    if (lane == 0)
+                        *reinterpret_cast<volatile int32_t *>(abort_word) = 1;
+                    named_barrier_sync(1, NC);
+                }
+                report(p.status, MOE_ERR_DEVICE_TIMEOUT);
+            };
             // gamma's slice, copied to shared memory once by the producer
             if (do_norm && __any_sync(0xffffffffu, !mbar_wait_bounded(gbar, 0, kWaitLimitNs))) {
-                report(p.status, MOE_ERR_DEVICE_TIMEOUT);
+                give_up();
                 return;
             }
 
@@ -436,7 +457,7 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                     // a give-up is taken by the whole warp, so that no lane is
                     // left behind in the warp-wide shuffles below
                     if (__any_sync(0xffffffffu, !mbar_wait_bounded(full0 + 8u * stage, phase, kWaitLimitNs))) {
-                        report(p.status, MOE_ERR_DEVICE_TIMEOUT);
+                        give_up();
                         return;
                     }
                     // the slot's header (t, n, flags) in one 16-byte load
@@ -542,6 +563,7 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                         ss += __shfl_xor_sync(0xffffffffu, ss, d);
                     const float *part;
                     int np;
+                    int32_t aborted = 0;
                     if constexpr (SPLIT) {
                         // every warp of every CTA of the cluster sends its partial
                         // to slot [rank][warp] of every CTA (lane r to CTA r) and
@@ -566,14 +588,10 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                         np = static_cast<int>(csize) * ncw;
                     } else {
                         float *mine = red + (tok & 1u) * ncw;
-                        if (lane == 0) {
+                        if (lane == 0)
                             mine[warp] = ss;
-                            mbar_arrive(redbar);
-                        }
-                        if (__any_sync(0xffffffffu, !mbar_wait_bounded(redbar, tok & 1u, kWaitLimitNs))) {
-                            report(p.status, MOE_ERR_DEVICE_TIMEOUT);
-                            return;
-                        }
+                        named_barrier_sync(1, NC);  // the consumer warps only
+                        aborted = *abort_word;      // checked before the next store
                         part = mine;
                         np = ncw;
                     }
@@ -599,6 +617,8 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                             acc[s][2 * i + 1] = acc[s][2 * i + 1] * rinv * (hi + p.wb);
                         }
                     }
+                    if (aborted)  // a warp gave up (and has reported)
+                        return;
                     if (p.norm_out) {
 #pragma unroll
                         for (int s = 0; s < VPT; ++s) {

@@ -83,6 +83,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Hardware barrier `id` (1..15; 0 is __syncthreads) for `count` threads of
+// the CTA (a multiple of 32); every participating thread must reach it.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------------ thread-block clusters
 
 __device__ __forceinline__ uint32_t cluster_rank()
