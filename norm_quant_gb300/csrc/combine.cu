@@ -36,7 +36,8 @@
 //     load, before its sums), accumulate fp32 in row order, and release the
 //     slot on its "empty" mbarrier;
 //   * after a token's last slot: bf16 stores, a sum of squares reduced by
-//     warp shuffles and an mbarrier-synchronised cross-warp sum, the norm,
+//     warp shuffles and a cross-warp sum at a named barrier of the
+//     consumer warps, the norm,
 //     and the block quantiser (an MXFP8 block is 4 consecutive lanes, NVFP4 2);
 //   * on request (moe_tuning_set), a token is split by columns over a
 //     thread-block cluster of 2..16 CTAs (each copies, sums, normalises and
@@ -47,8 +48,10 @@
 //   * gamma's slice is copied to shared memory once per CTA, and the
 //     per-warp partial sums of squares are added by a butterfly that gives
 //     every lane the same total.
-// Every wait is bounded (kWaitLimitNs); a wait that gives up records
-// MOE_ERR_DEVICE_TIMEOUT and the CTA drains its own copies and finishes.
+// Every mbarrier wait is bounded (kWaitLimitNs); a wait that gives up records
+// MOE_ERR_DEVICE_TIMEOUT and the CTA drains its own copies and finishes (a
+// consumer warp that gives up first meets the others at the norm's barrier
+// with an abort flag, so that none waits there forever).
 #include <cstdint>
 #include <cuda_runtime.h>
 
