@@ -97,7 +97,9 @@ typedef enum {
 } moe_io_dtype;
 
 /* Element type of router_weights (Struct_ep_combine_skip_a2a --
- * router_weights_dtype); weights are widened to fp32 exactly. */
+ * router_weights_dtype); weights are widened to fp32 exactly.  fp16 weights
+ * with fp16 I/O take a kernel that multiplies the fp16 row elements by the
+ * fp16 weight directly (the product is exact in fp32): the same results. */
 typedef enum {
     MOE_WEIGHTS_FP32 = 0,
     MOE_WEIGHTS_BF16 = 1,

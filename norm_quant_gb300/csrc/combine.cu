@@ -17,7 +17,9 @@
 //   MXFP4: per 32 elements, e = smallest integer with amax <= 6 * 2^e,
 //          byte = clamp(e + 127, 0, 254), code = e2m1_rn_sat(y * 2^-e)
 // Inputs and outputs are bf16 or fp16 (io_dtype); router weights fp32,
-// bf16 or fp16 (weight_dtype); accumulation is fp32 throughout.
+// bf16 or fp16 (weight_dtype); accumulation is fp32 throughout.  With fp16
+// rows and fp16 weights each product is formed by a mixed-precision fma
+// (fp16 x fp16 + fp32), which is exact, so the result is the same bits.
 //
 // Design (an HBM-bound gather; no tensor cores -- nothing here is a
 // contraction):
@@ -64,6 +66,7 @@ Tuning g_tuning;
 
 // the fp16 kernels are instantiated in combine_f16.cu
 extern template moe_status launch_io<1>(const Params &, const Plan &, int32_t, cudaStream_t);
+extern template moe_status launch_io<2>(const Params &, const Plan &, int32_t, cudaStream_t);
 template moe_status launch_io<0>(const Params &, const Plan &, int32_t, cudaStream_t);
 
 } // namespace combine_detail
@@ -193,7 +196,11 @@ extern "C" moe_status moe_combine(const moe_combine_args *a, moe_stream_t stream
         p.split = pl.split;
         p.hl = pl.hl;
         p.stall_after = g_tuning.stall_after;
-        return a->io_dtype == MOE_IO_FP16 ? launch_io<1>(p, pl, a->quant, s) : launch_io<0>(p, pl, a->quant, s);
+        if (a->io_dtype == MOE_IO_BF16)
+            return launch_io<0>(p, pl, a->quant, s);
+        // fp16 rows with fp16 weights: products exact without widening the rows
+        return a->weight_dtype == MOE_WEIGHTS_FP16 ? launch_io<2>(p, pl, a->quant, s)
+                                                   : launch_io<1>(p, pl, a->quant, s);
     };
     // rows a token may need: its valid expert rows, the shared row, the residual row
     const int rows_per_token = a->top_k + (a->shared_out ? 1 : 0) + (a->residual ? 1 : 0);

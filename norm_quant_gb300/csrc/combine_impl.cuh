@@ -117,7 +117,9 @@ __device__ __forceinline__ int32_t ue8m0_byte(float amax)
     return b < 0 ? 0 : (b > 254 ? 254 : b);
 }
 
-// 16-bit element codecs: IO 0 = bf16, 1 = fp16.
+// 16-bit element codecs.  IO 0 = bf16; 1 = fp16; 2 = fp16 with fp16 router
+// weights (the same codecs as 1; only the weighted sum differs: the rows are
+// not widened, each element takes one mixed-precision fma).
 template <int IO>
 __device__ __forceinline__ void unpack16x2(uint32_t w, float &lo, float &hi)
 {
@@ -505,11 +507,20 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                                 const int v = s * NC + tid;
                                 if (v < nvec) {
                                     const uint32_t qw[4] = {q[rr][s].x, q[rr][s].y, q[rr][s].z, q[rr][s].w};
+                                    if constexpr (IO == 2) {
+                                        // the weight is an fp16 number (or the
+                                        // 1 of the shared / residual row)
+                                        const unsigned short wh = f32_to_f16_bits(wr[rr]);
 #pragma unroll
-                                    for (int i = 0; i < 4; ++i) {
-                                        float lo, hi;
-                                        unpack16x2<IO>(qw[i], lo, hi);
-                                        fma2(acc[s][2 * i], acc[s][2 * i + 1], lo, hi, wr[rr]);
+                                        for (int i = 0; i < 4; ++i)
+                                            fma2_f16(acc[s][2 * i], acc[s][2 * i + 1], qw[i], wh);
+                                    } else {
+#pragma unroll
+                                        for (int i = 0; i < 4; ++i) {
+                                            float lo, hi;
+                                            unpack16x2<IO>(qw[i], lo, hi);
+                                            fma2(acc[s][2 * i], acc[s][2 * i + 1], lo, hi, wr[rr]);
+                                        }
                                     }
                                 }
                             }
@@ -954,8 +965,9 @@ moe_status launch_q(const Params &p, const Plan &pl, cudaStream_t stream)
     }
 }
 
-// Every kernel of one 16-bit I/O type; each type is compiled in its own
-// translation unit (combine.cu: bf16, combine_f16.cu: fp16).
+// Every kernel of one I/O form; each form is compiled in its own translation
+// unit (combine.cu: bf16, combine_f16.cu: fp16, combine_f16w.cu: fp16 with
+// fp16 router weights).
 template <int IO>
 moe_status launch_io(const Params &p, const Plan &pl, int32_t quant, cudaStream_t stream)
 {

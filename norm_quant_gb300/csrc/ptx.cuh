@@ -312,6 +312,30 @@ __device__ __forceinline__ void fma2(float &acc_lo, float &acc_hi, float x_lo, f
     asm("mov.b64 {%0, %1}, %2;" : "=f"(acc_lo), "=f"(acc_hi) : "l"(a));
 }
 
+// fp32 -> fp16 bits, round to nearest even (exact for a value that is an
+// fp16 number, such as a router weight stored as fp16).
+__device__ __forceinline__ unsigned short f32_to_f16_bits(float x)
+{
+    unsigned short r;
+    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(x));
+    return r;
+}
+
+// acc_lo += lo(x) * w and acc_hi += hi(x) * w for an fp16 pair x (a 32-bit
+// word) and an fp16 weight w, without widening x: the mixed-precision fma
+// (fp16 multiplicands, fp32 addend and result; PTX ISA 8.6, sm_100 and
+// later).  A product of two fp16 numbers is exact in fp32, so each lane
+// rounds once, as fmaf of the widened operands does.
+__device__ __forceinline__ void fma2_f16(float &acc_lo, float &acc_hi, uint32_t x, unsigned short w)
+{
+    asm("{ .reg .b16 l, h;\n"
+        "  mov.b32 {l, h}, %2;\n"
+        "  fma.rn.f32.f16 %0, l, %3, %0;\n"
+        "  fma.rn.f32.f16 %1, h, %3, %1; }"
+        : "+f"(acc_lo), "+f"(acc_hi)
+        : "r"(x), "h"(w));
+}
+
 // Two fp32 -> bf16x2, round to nearest even; `lo` in the low half.
 __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi)
 {

@@ -420,6 +420,56 @@ def test_dtype_and_mxfp4_parity(kw):
     compare(wl, inp, orm, got, global_scale=g)
 
 
+
+def _f16_edge_inputs(wl, seed):
+    """fp16 inputs with the values an unwidened fp16 product must get right:
+    subnormal and large row elements, negative zeros, and subnormal, negative
+    and greater-than-one fp16 router weights."""
+    inp = synth.make_inputs(wl)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ex = inp["expert_out"].copy()
+    u = rng.random(ex.shape)
+    sign = (rng.integers(0, 2, ex.shape) << 15).astype(np.uint16)
+    sub = rng.integers(1, 0x400, ex.shape).astype(np.uint16) | sign       # subnormal
+    big = rng.integers(0x6400, 0x6C00, ex.shape).astype(np.uint16) | sign  # [1024, 4096)
+    ex = np.where(u < 0.02, sub, np.where(u < 0.03, big, np.where(u < 0.035, np.uint16(0x8000), ex)))
+    inp["expert_out"] = ex.astype(np.uint16)
+    w = inp["weights"].copy()
+    v = rng.random(w.shape)
+    w = np.where(v < 0.1, rng.integers(1, 0x400, w.shape).astype(np.uint16),  # subnormal weight
+                 np.where(v < 0.15, np.uint16(0x4300),                         # 3.5
+                          np.where(v < 0.2, np.uint16(0xBA00), w)))            # -0.75
+    inp["weights"] = w.astype(np.uint16)
+    return inp
+
+
+@pytest.mark.parametrize("plan", [None, (1, 3, 0), (2, 8, 0), (4, 6, 0), (8, 12, 0), (0, 0, 2), (0, 0, 4)],
+                         ids=["auto", "vpt1_r3", "vpt2_r8", "vpt4_r6", "vpt8_r12", "split2", "split4"])
+def test_fp16_weights_kernel_matches_widening_bit_for_bit(plan):
+    """fp16 rows with fp16 weights run a kernel that multiplies without
+    widening (mixed-precision fma).  On edge values it agrees with the
+    oracle, and bit for bit with the widening kernel given the same weights
+    as fp32, in every launch plan."""
+    wl = _wl(T=37, H=2048, k=8, E=64, shared_std=0.5, io_dtype="fp16", weight_dtype="fp16",
+             quant="mxfp8", outputs=("combined", "residual", "norm", "quant"), seed=91)
+    inp = _f16_edge_inputs(wl, seed=92)
+    d_rm, orm = route_and_check(inp["topk_ids"], wl.E)
+    wl32 = dataclasses.replace(wl, weight_dtype="fp32")
+    inp32 = dict(inp, weights=inp["weights"].view(np.float16).astype(np.float32))
+    try:
+        if plan is not None:
+            vpt, rows, split = plan
+            nqg.moe_tuning_set(vpt, rows, 0, 0, 0, split)
+        got = gpu_combine(wl, inp, d_rm, canary=True)
+        ref = gpu_combine(wl32, inp32, d_rm, canary=True)
+    finally:
+        nqg.moe_tuning_set()
+    assert got["status"] == 0 and ref["status"] == 0
+    for name in ("combined", "residual", "norm", "quant", "scales"):
+        assert np.array_equal(got[name], ref[name]), name
+    compare(wl, inp, orm, got)
+
+
 # ------------------------------------------------- split rows (decode sizes)
 
 SPLIT_CASES = [
