@@ -44,7 +44,9 @@ FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = ["norm_quant_gb300/csrc/combine.cu", "norm_quant_gb300/csrc/combine_impl.cuh",
                   "norm_quant_gb300/csrc/ptx.cuh"]
-TRAFFIC_FILE = "profiles/combine_prefill_T4096_H7168_k8_mxfp8.md"
+# the committed ncu summary of each workload whose combine traffic was captured
+TRAFFIC_FILES = {"prefill": "profiles/combine_prefill_T4096_H7168_k8_mxfp8.md",
+                 "fp16": "profiles/combine_prefill_fp16io_fp16weights_T4096_H7168_k8_mxfp8.md"}
 
 
 def parse():
@@ -144,11 +146,15 @@ def kernel_hash(read=None) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per combine launch from the committed ncu summary, or None
-    if the kernel source changed since those counters were taken."""
+def recorded_traffic(kind="prefill", read=None):
+    """DRAM bytes per combine launch from the workload's committed ncu
+    summary, or None if there is none or the kernel source changed since
+    those counters were taken."""
+    read = read or (lambda f: open(os.path.join(ROOT, f)).read())
+    if kind not in TRAFFIC_FILES:
+        return None
     try:
-        text = open(os.path.join(ROOT, TRAFFIC_FILE)).read()
+        text = read(TRAFFIC_FILES[kind])
     except OSError:
         return None
     m = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
@@ -587,7 +593,7 @@ def run_ours(args):
                          "kernel": "dispatch_kernel" if kind == "dispatch" else "combine_kernel",
                          "kernel_ms": comb_avg_s * 1e3,
                          "algorithmic_bytes": byt["total"],
-                         "traffic": recorded_traffic() if kind == "prefill" else None},
+                         "traffic": recorded_traffic(kind)},
             "e2e": {"value": job_throughput(world, T, args.e2e_steps, e2e_s), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": (route_kernels + 1) * K,

@@ -5,6 +5,8 @@ the shared and residual rows, 8k bytes of row_map and weights per token and
 gamma once; writes of each 16-bit output, the fp8 / fp4 codes and the scale
 bytes), and the code-only source hash that decides whether a recorded ncu
 traffic figure still applies."""
+import os
+
 import pytest
 
 import bench
@@ -51,3 +53,17 @@ def test_kernel_hash_changes_with_code_not_with_comments():
     assert bench.kernel_hash(lambda f: commented[f]) == h0
     edited = dict(src, **{first: src[first] + "\nstatic int extra_symbol = 1;\n"})
     assert bench.kernel_hash(lambda f: edited[f]) != h0
+
+
+def test_recorded_traffic_needs_a_matching_source_hash():
+    """A summary's DRAM bytes count only while its hash is the kernel
+    sources' hash; workloads without a summary report none."""
+    h = bench.kernel_hash()
+    summary = {f: f"x\ndram_bytes_per_launch: 123456\nkernel_source_hash: {h}\n"
+               for f in bench.TRAFFIC_FILES.values()}
+    assert bench.recorded_traffic("prefill", summary.__getitem__) == 123456
+    assert bench.recorded_traffic("fp16", summary.__getitem__) == 123456
+    assert bench.recorded_traffic("gemma", summary.__getitem__) is None
+    stale = {f: t.replace(h, "0" * 16) for f, t in summary.items()}
+    assert bench.recorded_traffic("prefill", stale.__getitem__) is None
+    assert all(os.path.exists(os.path.join(bench.ROOT, f)) for f in bench.TRAFFIC_FILES.values())
