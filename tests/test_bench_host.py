@@ -63,7 +63,8 @@ def test_recorded_traffic_needs_a_matching_source_hash():
                for f in bench.TRAFFIC_FILES.values()}
     assert bench.recorded_traffic("prefill", summary.__getitem__) == 123456
     assert bench.recorded_traffic("fp16", summary.__getitem__) == 123456
-    assert bench.recorded_traffic("gemma", summary.__getitem__) is None
+    assert bench.recorded_traffic("gemma", summary.__getitem__) == 123456
+    assert bench.recorded_traffic("decode", summary.__getitem__) is None
     stale = {f: t.replace(h, "0" * 16) for f, t in summary.items()}
     assert bench.recorded_traffic("prefill", stale.__getitem__) is None
     assert all(os.path.exists(os.path.join(bench.ROOT, f)) for f in bench.TRAFFIC_FILES.values())
