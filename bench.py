@@ -42,8 +42,10 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE combine tokens/s and achieved HBM GB/s vs peak (T=4096,H=7168,k=8)"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
+# every source the combine kernels are compiled from
 KERNEL_SOURCES = ["norm_quant_gb300/csrc/combine.cu", "norm_quant_gb300/csrc/combine_impl.cuh",
-                  "norm_quant_gb300/csrc/ptx.cuh"]
+                  "norm_quant_gb300/csrc/ptx.cuh", "norm_quant_gb300/csrc/combine_f16.cu",
+                  "norm_quant_gb300/csrc/combine_f16w.cu", "norm_quant_gb300/csrc/common.h"]
 # the committed ncu summary of each workload whose combine traffic was captured
 TRAFFIC_FILES = {"prefill": "profiles/combine_prefill_T4096_H7168_k8_mxfp8.md",
                  "fp16": "profiles/combine_prefill_fp16io_fp16weights_T4096_H7168_k8_mxfp8.md",
