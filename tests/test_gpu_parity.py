@@ -470,6 +470,42 @@ def test_fp16_weights_kernel_matches_widening_bit_for_bit(plan):
     compare(wl, inp, orm, got)
 
 
+
+@pytest.mark.parametrize("io,wdt", [("fp16", "fp32"), ("fp16", "fp16"), ("bf16", "fp32"), ("bf16", "bf16")])
+def test_pure_gather_returns_every_finite_code(io, wdt):
+    """top_k = 1 with weight 1, no other rows and no norm: the combined
+    output is the expert row itself, so every finite 16-bit code (all 63,488
+    of fp16, all 65,280 of bf16) comes back unchanged, except -0, which
+    becomes +0 (the sum starts from +0).  This checks the widening of rows
+    and weights and the rounding back, exhaustively."""
+    H = 2048 if io == "fp16" else 256
+    n_exp = 31 if io == "fp16" else 255             # biased exponents of the finite codes
+    mant = 1024 if io == "fp16" else 128
+    shift = 10 if io == "fp16" else 7
+    e = np.repeat(np.arange(n_exp, dtype=np.uint32), 2 * mant)
+    m = np.tile(np.arange(mant, dtype=np.uint32), 2 * n_exp)
+    sg = np.tile(np.repeat(np.array([0, 0x8000], np.uint32), mant), n_exp)
+    codes = (sg | (e << shift) | m).astype(np.uint16).reshape(n_exp, H)
+    T = n_exp
+    one = {"fp32": np.float32(1.0), "fp16": np.uint16(0x3C00), "bf16": np.uint16(0x3F80)}[wdt]
+    weights = np.full((T, 1), one)
+    ids = np.zeros((T, 1), np.int32)
+    d_rm, orm = route_and_check(ids, 1)
+    rows = np.empty_like(codes)
+    rows[orm[:, 0]] = codes                          # expert row row_map[t] holds token t's codes
+    ex = torch.from_numpy(rows.view(np.int16)).cuda()
+    out = torch.full((T, H), 0x5A5A, dtype=torch.int16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nqg.moe_combine(expert_out=ex, row_map=d_rm, router_weights=torch.from_numpy(weights).cuda(),
+                    combined_out=out, status=status, H=H, io_dtype=io, weight_dtype=wdt)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    want = np.where(codes == 0x8000, np.uint16(0), codes)
+    got = h(out, np.uint16)
+    bad = got != want
+    assert not bad.any(), [(hex(int(want[i])), hex(int(got[i]))) for i in map(tuple, np.argwhere(bad)[:5])]
+
+
 # ------------------------------------------------- split rows (decode sizes)
 
 SPLIT_CASES = [
