@@ -62,11 +62,12 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", choices=["tiny", "decode", "prefill", "gemma", "padded",
-                                           "slot_major", "dispatch", "mxfp4", "fp16"],
+                                           "slot_major", "dispatch", "mxfp4", "fp16", "fp16_fp32w"],
                     default="prefill", help="the headline is prefill; the others are for analysis "
                     "(slot_major: the prefill shape with [k, T, H] expert rows; dispatch: the "
                     "prefill shape's dispatch-side permute; mxfp4: the prefill shape with MXFP4 "
-                    "output; fp16: the prefill shape with fp16 inputs, outputs and router weights)")
+                    "output; fp16: the prefill shape with fp16 inputs, outputs and router weights; fp16_fp32w: "
+                    "the same with fp32 router weights)")
     ap.add_argument("--l2", choices=["none", "write"], default="none",
                     help="none: inputs larger than L2; write: 256 MB write before each step")
     return ap.parse_args()
@@ -103,7 +104,9 @@ def workload(name="prefill"):
             "gemma": synth.GEMMA_NVFP4, "padded": synth.PADDED, "slot_major": P, "dispatch": P,
             "mxfp4": dataclasses.replace(P, quant="mxfp4", name=P.name.replace("mxfp8", "mxfp4")),
             "fp16": dataclasses.replace(P, io_dtype="fp16", weight_dtype="fp16",
-                                        name=P.name.replace("rmsnorm", "fp16io_fp16weights_rmsnorm"))}[name]
+                                        name=P.name.replace("rmsnorm", "fp16io_fp16weights_rmsnorm")),
+            "fp16_fp32w": dataclasses.replace(P, io_dtype="fp16",
+                                              name=P.name.replace("rmsnorm", "fp16io_rmsnorm"))}[name]
 
 
 def algorithmic_bytes(wl, n_valid: int) -> dict:
