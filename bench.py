@@ -109,20 +109,24 @@ def workload(name="prefill"):
                                               name=P.name.replace("rmsnorm", "fp16io_rmsnorm"))}[name]
 
 
-def algorithmic_bytes(wl, n_valid: int) -> dict:
-    """Bytes one combine launch must move at least (reads + writes)."""
+def algorithmic_bytes(wl, n_valid: int, expert_layout: str = "grouped") -> dict:
+    """Bytes one combine launch must move at least (reads + writes).  The
+    slot-major layout reads no row_map; 128x4 scales include their pad bytes
+    (rows to a multiple of 128, scale columns to a multiple of 4)."""
     T, H, k = wl.T, wl.H, wl.k
     rows = n_valid * 2 * H
     other = (2 * H * T if wl.shared_std is not None else 0) + (2 * H * T if wl.residual else 0)
     weight_bytes = 4 if wl.weight_dtype == "fp32" else 2
-    meta = (4 + weight_bytes) * k * T + (2 * H if wl.gamma_mean is not None else 0)
+    map_bytes = 0 if expert_layout == "slot_major" else 4
+    meta = (map_bytes + weight_bytes) * k * T + (2 * H if wl.gamma_mean is not None else 0)
     writes = 2 * H * T * len([o for o in wl.outputs if o in ("combined", "residual", "norm")])
-    if wl.quant == "mxfp8":
-        writes += H * T + H // 32 * T
-    elif wl.quant == "nvfp4":
-        writes += H // 2 * T + H // 16 * T
-    elif wl.quant == "mxfp4":
-        writes += H // 2 * T + H // 32 * T
+    if wl.quant:
+        writes += (H if wl.quant == "mxfp8" else H // 2) * T           # codes
+        cols = H // (16 if wl.quant == "nvfp4" else 32)
+        if wl.sf_layout == "swizzled":
+            writes += -(-T // 128) * 128 * (-(-cols // 4) * 4)
+        else:
+            writes += cols * T
     return {"rows": rows, "other_reads": other, "meta": meta, "writes": writes,
             "total": rows + other + meta + writes}
 
@@ -571,7 +575,7 @@ def run_ours(args):
             nv = inp["n_valid"]
             byt = {"total": T * 2 * H + nv * 2 * H + 4 * k * T}
         else:
-            byt = algorithmic_bytes(wl, inp["n_valid"])
+            byt = algorithmic_bytes(wl, inp["n_valid"], "slot_major" if kind == "slot_major" else "grouped")
         comb_avg_s = comb_s
         achieved = byt["total"] / comb_avg_s / 1e9
         peak, peak_kind = measured_peak()

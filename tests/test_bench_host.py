@@ -37,6 +37,25 @@ def test_byte_count_follows_dtypes_and_formats():
     assert base["rows"] == fp16["rows"] == mxfp4["rows"] == 32768 * 2 * H
 
 
+def test_byte_count_follows_layouts():
+    """Slot-major reads no row_map; 128x4 scales count their pad bytes,
+    as the library sizes them (checked against the oracle's sizes)."""
+    import dataclasses
+    import oracle
+    P = bench.workload("prefill")
+    grouped = bench.algorithmic_bytes(P, 32768)
+    slot = bench.algorithmic_bytes(P, 32768, "slot_major")
+    assert grouped["meta"] - slot["meta"] == 4 * P.k * P.T
+    for q in ("mxfp8", "nvfp4", "mxfp4"):
+        for T, H in ((4096, 7168), (300, 96), (130, 224)):
+            wl = dataclasses.replace(P, T=T, H=H, quant=q, sf_layout="swizzled", outputs=("quant",))
+            codes = (H if q == "mxfp8" else H // 2) * T
+            assert bench.algorithmic_bytes(wl, 8 * T)["writes"] == \
+                codes + oracle.scales_bytes(T, H, q, "swizzled")
+            wl = dataclasses.replace(wl, sf_layout="linear")
+            assert bench.algorithmic_bytes(wl, 8 * T)["writes"] == codes + oracle.scales_bytes(T, H, q, "linear")
+
+
 def test_code_only_ignores_comments_and_whitespace():
     a = "int f(int x) { // add one\n  return x + 1; /* block\n comment */ }\n"
     b = "int f(int x)\n{\n    return x + 1;\n}"
