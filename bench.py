@@ -262,8 +262,9 @@ def _pool_slice(bounds):
     oracle.combine(A["expert_out"], A["row_map"][a:b], A["weights"][a:b],
                    shared=A["shared"][a:b] if "shared" in A else None,
                    residual=A["residual"][a:b] if "residual" in A else None, gamma=A.get("gamma"),
-                   eps=P["eps"], weight_bias=P["weight_bias"], quant=P["quant"], sf_layout="linear",
-                   outputs=("residual", "quant"))
+                   eps=P["eps"], weight_bias=P["weight_bias"], quant=P["quant"],
+                   sf_layout=P["sf_layout"], outputs=P["outputs"], io_dtype=P["io_dtype"],
+                   weight_dtype=P["weight_dtype"])
     return b - a
 
 
@@ -288,7 +289,9 @@ class OraclePool:
             np.ndarray(arr.shape, dtype=arr.dtype, buffer=shm.buf)[...] = arr
             self.shms.append(shm)
             specs[name] = (shm.name, arr.shape, arr.dtype.str)
-        params = {"E": wl.E, "eps": wl.eps, "weight_bias": wl.weight_bias, "quant": wl.quant}
+        params = {"E": wl.E, "eps": wl.eps, "weight_bias": wl.weight_bias, "quant": wl.quant,
+                  "sf_layout": wl.sf_layout, "outputs": tuple(wl.outputs), "io_dtype": wl.io_dtype,
+                  "weight_dtype": wl.weight_dtype}
         self.pool = mp.get_context("spawn").Pool(self.workers, initializer=_pool_init, initargs=(specs, params))
         self.pool.map(_pool_slice, [(0, 1)] * self.workers)  # every worker started and warm
 
@@ -323,13 +326,17 @@ def cpu_oracle_rate_all_cores(wl, inp, orm, seconds: float):
 
 def run_reference(args):
     """The reference arm: the CPU oracle timed as it stands, on all host cores
-    (token slices in spawned processes)."""
+    (token slices in spawned processes), on the same workload as our arm
+    (the headline unless --workload names another routing + combine one)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
+    if args.workload in ("slot_major", "dispatch"):
+        raise SystemExit(f"bench.py --impl reference times the routing build + combine workloads; "
+                         f"--workload {args.workload} has no reference arm")
     import oracle
     from norm_quant_gb300 import synth
-    wl = workload("prefill")  # the reference arm always times the headline workload
+    wl = workload(args.workload)
     inp = synth.make_inputs(wl)
     st, _, _, orm, _ = oracle.build_row_map(inp["topk_ids"], wl.E)
     pool = OraclePool(wl, inp, orm)

@@ -87,3 +87,38 @@ def test_recorded_traffic_needs_a_matching_source_hash():
     stale = {f: t.replace(h, "0" * 16) for f, t in summary.items()}
     assert bench.recorded_traffic("prefill", stale.__getitem__) is None
     assert all(os.path.exists(os.path.join(bench.ROOT, f)) for f in bench.TRAFFIC_FILES.values())
+
+
+def _reference_arm(*extra, env=None):
+    import json
+    import subprocess
+    import sys
+    run = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "3", "--warmup", "3",
+                          *extra], cwd=bench.ROOT, capture_output=True, text=True, timeout=600,
+                         env={**os.environ, **(env or {})})
+    lines = [json.loads(x) for x in run.stdout.splitlines() if x.startswith("{")]
+    return run.returncode, lines, run.stderr
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_reference_arm_line(name):
+    """The oracle arm on the CPU: one JSON line with the contract's keys, on
+    the requested workload, with no host<->device bytes."""
+    rc, lines, err = _reference_arm("--workload", name)
+    assert rc == 0, err[-2000:]
+    assert len(lines) == 1
+    line = lines[0]
+    wl = bench.workload(name)
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["config"]["workload"] == wl.name and line["config"]["T"] == wl.T
+    assert line["value"] > 0 and line["unit"] == "tokens/s" and line["higher_is_better"] is True
+    assert line["steps"] == 3 and line["warmup"] == 3 and line["dtype"] == "f64"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s",
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    rc, lines, _ = _reference_arm("--workload", "tiny", env={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert rc == 0 and lines == []
