@@ -32,8 +32,12 @@ def test_fp16_products_are_exact_in_fp32():
     rng = np.random.Generator(np.random.PCG64(1616))
     a = rng.choice(x, 2_000_000)
     b = rng.choice(x, 2_000_000)
-    # the extremes and the subnormals, all against all
-    ends = np.concatenate([x[np.abs(x.astype(np.float64)) < 2.0 ** -14], x[np.abs(x) >= 32768]])
+    # the subnormals and the largest binade (every fourth code, plus the
+    # endpoints 2^-24, the largest subnormal, 2^-14 and 65504), all against all
+    sub = x[np.abs(x.astype(np.float64)) < 2.0 ** -14]
+    top = x[np.abs(x) >= 32768]
+    edge = np.array([2.0 ** -24, 1023 * 2.0 ** -24, 2.0 ** -14, 65504.0], np.float16)
+    ends = np.concatenate([sub[::4], top[::4], edge, -edge])
     a = np.concatenate([a, np.repeat(ends, ends.size)])
     b = np.concatenate([b, np.tile(ends, ends.size)])
     p32 = a.astype(np.float32) * b.astype(np.float32)
