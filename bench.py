@@ -68,6 +68,8 @@ def parse():
                     "prefill shape's dispatch-side permute; mxfp4: the prefill shape with MXFP4 "
                     "output; fp16: the prefill shape with fp16 inputs, outputs and router weights; fp16_fp32w: "
                     "the same with fp32 router weights)")
+    ap.add_argument("--T", type=int, default=None,
+                    help="with --workload padded: a point of its token-count sweep (seed 2000 + T)")
     ap.add_argument("--l2", choices=["none", "write"], default="none",
                     help="none: inputs larger than L2; write: 256 MB write before each step")
     return ap.parse_args()
@@ -94,6 +96,17 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def args_workload(args):
+    """The workload the command line names: --workload, or a point of the
+    padded workload's token-count sweep with --T."""
+    from norm_quant_gb300 import synth
+    if args.T is None:
+        return workload(args.workload)
+    if args.workload != "padded" or args.T < 1:
+        raise SystemExit("bench.py: --T takes a positive token count and goes with --workload padded")
+    return synth.sweep_point(args.T)
 
 
 def workload(name="prefill"):
@@ -336,7 +349,7 @@ def run_reference(args):
                          f"--workload {args.workload} has no reference arm")
     import oracle
     from norm_quant_gb300 import synth
-    wl = workload(args.workload)
+    wl = args_workload(args)
     inp = synth.make_inputs(wl)
     st, _, _, orm, _ = oracle.build_row_map(inp["topk_ids"], wl.E)
     pool = OraclePool(wl, inp, orm)
@@ -396,7 +409,7 @@ def run_ours(args):
     nqg.lib()
 
     kind = args.workload
-    wl = workload(kind)
+    wl = args_workload(args)
     T, H, E, k = wl.T, wl.H, wl.E, wl.k
     inp = synth.make_slot_major_inputs(wl) if kind == "slot_major" else synth.make_inputs(wl)
     if kind == "dispatch":  # the residual stream is the token input of the permute
@@ -490,6 +503,7 @@ def run_ours(args):
         return g
 
     g_step, g_comb = graph_of(step, G), graph_of(combine, G)
+    g_route = graph_of(route, G) if kind != "slot_major" else None
 
     replay_s = []  # device seconds of each replay of the last replay() call
 
@@ -529,6 +543,7 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
         comb_s = replay(g_comb, K // G) / K    # the combine kernel alone, same count
+        route_s = replay(g_route, K // G) / K if g_route is not None else None  # the routing build alone
     total_s = max_over_ranks(total_s, dev)
 
     # end to end through the C ABI from pinned host buffers: every step copies
@@ -602,7 +617,8 @@ def run_ours(args):
                               f"no flush: each step streams {byt['total'] / 1e6:.0f} MB through the 129 MB L2"),
                        "timing": f"K steps (routing build + combine) as K/{G} replays of a CUDA graph of "
                                  f"{G} consecutive steps, between two events; the roofline times the same "
-                                 f"count of combine launches in graphs of {G}",
+                                 f"count of combine launches in graphs of {G}, and route_us the routing "
+                                 f"build alone the same way",
                        "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
             "achieved_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -614,6 +630,7 @@ def run_ours(args):
             "e2e": {"value": job_throughput(world, T, args.e2e_steps, e2e_s), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": (route_kernels + 1) * K,
+            "route_us": route_s * 1e6 if route_s is not None else None,
             "step_time_us": {"p10": float(step_pct[0]), "p50": float(step_pct[1]), "p90": float(step_pct[2]),
                              "over": f"{K // G} replays of {G} steps each (rank {rank})"},
             "clocks": clk.summary(),
