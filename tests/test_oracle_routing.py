@@ -73,3 +73,14 @@ def test_routing_invalid_ids_are_flagged_and_padded():
     assert st == 4
     assert row_map[0, 0] == -1 and row_map[-1, -1] == -1
     assert counts.sum() == int(((ids >= 0) & (ids < 6)).sum())
+
+
+@pytest.mark.parametrize("bad", [6, 7, 1000, -2, -1000])
+def test_each_kind_of_invalid_id_is_flagged_on_its_own(bad):
+    """An id at or above E, or below -1, is reported even when it is the
+    only invalid one; -1 alone is padding and is not."""
+    ids = np.array([[0, 5], [bad, 1], [-1, 2]], np.int32)
+    st, counts, _, row_map, _ = oracle.build_row_map(ids, 6)
+    assert st == 4 and row_map[1, 0] == -1 and counts.sum() == 4
+    st, _, _, _, _ = oracle.build_row_map(np.where(ids == bad, -1, ids).astype(np.int32), 6)
+    assert st == 0
