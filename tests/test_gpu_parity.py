@@ -199,6 +199,26 @@ def test_invalid_expert_ids_are_flagged():
     assert h(counts).tolist() == [1, 1, 1, 0]
 
 
+@pytest.mark.parametrize("bad", ["E", "E+1000", "-2", "-1000"])
+@pytest.mark.parametrize("path", ["one_cta", "cluster", "three_kernels"])
+def test_each_kind_of_invalid_id_alone_on_every_routing_path(bad, path):
+    """One invalid id (at or above E, or below -1) among valid ones is
+    reported and treated as padding by each routing kernel; everything else
+    matches the oracle bit for bit."""
+    T, k, E = (64, 8, 256) if path == "one_cta" else (1024, 8, 256)
+    rng = np.random.Generator(np.random.PCG64(4040))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    ids[T // 2, k // 2] = {"E": E, "E+1000": E + 1000, "-2": -2, "-1000": -1000}[bad]
+    try:
+        nqg.moe_tuning_set(route_cluster=-1 if path == "three_kernels" else 0)
+        assert nqg.moe_build_row_map_launches(T, k, E) == (3 if path == "three_kernels" else 1)
+        route_and_check(ids, E)
+    finally:
+        nqg.moe_tuning_set()
+    ost = oracle.build_row_map(ids, E)[0]
+    assert ost == 4
+
+
 def test_empty_batch_is_a_noop():
     st, counts, offsets, row_map, _ = gpu_route(np.zeros((0, 4), np.int32), 8)
     assert st == 0 and h(counts).tolist() == [0] * 8 and h(offsets).tolist() == [0] * 9
