@@ -120,6 +120,23 @@ def _ptr(t):
     return t.data_ptr()
 
 
+def _need(t, nbytes: int, name: str):
+    """Raises ValueError if tensor t (when given) holds fewer than nbytes
+    bytes: the kernels take plain pointers and would read or write past a
+    buffer that is too small."""
+    if t is not None and t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes; this call needs {nbytes}")
+
+
+def _scales_bytes(T: int, H: int, vec: int, sf_layout: str) -> int:
+    """Bytes of a scale matrix: linear T x C, or 128x4 with rows padded to
+    128 and columns to 4 (the library's moe_scales_bytes)."""
+    cols = H // vec
+    if sf_layout == "linear":
+        return T * cols
+    return -(-T // 128) * 128 * (-(-cols // 4) * 4)
+
+
 def _stream(stream):
     if stream is None:
         import torch
@@ -145,6 +162,10 @@ def moe_build_row_map(topk_ids, E: int, counts, offsets, row_map, src_row=None,
     src_row [>= N_valid] (optional).  workspace: uint8 CUDA tensor of at least
     moe_build_row_map_workspace_size(T, k, E) bytes."""
     T, k = topk_ids.shape
+    _need(topk_ids, T * k * 4, "topk_ids")
+    _need(counts, E * 4, "counts")
+    _need(offsets, (E + 1) * 4, "offsets")
+    _need(row_map, T * k * 4, "row_map")
     _check(lib().moe_build_row_map(_ptr(topk_ids), T, k, E, _ptr(counts), _ptr(offsets),
                                    _ptr(row_map), _ptr(src_row), _ptr(workspace),
                                    workspace.numel() * workspace.element_size() if workspace is not None else 0,
@@ -158,6 +179,11 @@ def moe_build_row_map_noalloc(topk_ids, E: int, counts, offsets, row_map, src_ro
     allocate device memory: the library's own fixed scratch array is used
     (see include/moe_combine.h for its size limit and sharing rules)."""
     T, k = topk_ids.shape
+    _need(topk_ids, T * k * 4, "topk_ids")
+    _need(counts, E * 4, "counts")
+    _need(offsets, (E + 1) * 4, "offsets")
+    _need(row_map, T * k * 4, "row_map")
+    _need(error_flag, 4, "error_flag")
     _check(lib().moe_build_row_map_noalloc(_ptr(topk_ids), T, k, E, _ptr(counts), _ptr(offsets),
                                            _ptr(row_map), _ptr(src_row), _ptr(error_flag), _stream(stream)),
            "moe_build_row_map_noalloc")
@@ -184,6 +210,9 @@ def moe_scales_bytes(T: int, H: int, quant: str, sf_layout: str = "linear") -> i
 def moe_dispatch_permute(x, row_map, x_grouped, status=None, stream=None) -> None:
     """x [T, H] bf16 -> x_grouped [n_rows, H]: row row_map[t, j] >= 0 gets x[t]."""
     T, H = x.shape
+    _need(x, T * H * 2, "x")
+    _need(row_map, T * row_map.shape[1] * 4, "row_map")
+    _need(status, 4, "status")
     _check(lib().moe_dispatch_permute(_ptr(x), T, H, _ptr(row_map), row_map.shape[1], _ptr(x_grouped),
                                       int(x_grouped.shape[0]), _ptr(status), _stream(stream)),
            "moe_dispatch_permute")
@@ -215,6 +244,21 @@ def combine_args(*, expert_out, row_map, router_weights, shared_out=None, residu
     if H is None:
         H = int(expert_out.shape[-1])
     n_rows = int(expert_out.numel() // H) if H else 0
+    _need(router_weights, T * k * (4 if weight_dtype == "fp32" else 2), "router_weights")
+    if expert_layout == "slot_major":
+        _need(expert_out, k * T * H * 2, "expert_out")
+    else:
+        _need(row_map, T * k * 4, "row_map")
+    for name, t in (("shared_out", shared_out), ("residual", residual), ("combined_out", combined_out),
+                    ("residual_out", residual_out), ("norm_out", norm_out)):
+        _need(t, T * H * 2, name)
+    _need(gamma, H * 2, "gamma")
+    if quant:
+        _need(quant_out, T * (H if quant == "mxfp8" else H // 2), "quant_out")
+        vec = 16 if quant == "nvfp4" else 32
+        if H % vec == 0:  # otherwise the library rejects the call itself
+            _need(scales_out, _scales_bytes(T, H, vec, sf_layout), "scales_out")
+    _need(status, 4, "status")
     return MoeCombineArgs(
         T=T, H=H, top_k=k, expert_out=_ptr(expert_out), n_expert_rows=n_rows,
         expert_layout=EXPERT_LAYOUT[expert_layout],
