@@ -70,6 +70,8 @@ def parse():
                     "the same with fp32 router weights)")
     ap.add_argument("--T", type=int, default=None,
                     help="with --workload padded: a point of its token-count sweep (seed 2000 + T)")
+    ap.add_argument("--seed", type=int, default=None,
+                    help="another seed for the workload's synthetic inputs (default: the workload's own)")
     ap.add_argument("--l2", choices=["none", "write"], default="none",
                     help="none: inputs larger than L2; write: 256 MB write before each step")
     return ap.parse_args()
@@ -101,12 +103,17 @@ def dist_env():
 def args_workload(args):
     """The workload the command line names: --workload, or a point of the
     padded workload's token-count sweep with --T."""
+    import dataclasses
     from norm_quant_gb300 import synth
     if args.T is None:
-        return workload(args.workload)
-    if args.workload != "padded" or args.T < 1:
+        wl = workload(args.workload)
+    elif args.workload != "padded" or args.T < 1:
         raise SystemExit("bench.py: --T takes a positive token count and goes with --workload padded")
-    return synth.sweep_point(args.T)
+    else:
+        wl = synth.sweep_point(args.T)
+    if args.seed is not None:
+        wl = dataclasses.replace(wl, seed=args.seed, name=f"{wl.name}_seed{args.seed}")
+    return wl
 
 
 def workload(name="prefill"):

@@ -122,3 +122,22 @@ def test_reference_arm_line(name):
 def test_reference_arm_other_ranks_exit_quietly():
     rc, lines, _ = _reference_arm("--workload", "tiny", env={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert rc == 0 and lines == []
+
+
+def test_workload_from_the_command_line():
+    import sys
+    def parsed(*argv):
+        old = sys.argv
+        try:
+            sys.argv = ["bench.py", *argv]
+            return bench.args_workload(bench.parse())
+        finally:
+            sys.argv = old
+    assert parsed() == bench.workload("prefill")                       # the headline, unchanged
+    assert parsed("--workload", "gemma") == bench.workload("gemma")
+    w = parsed("--workload", "padded", "--T", "512")
+    assert (w.T, w.seed) == (512, 2512)
+    w = parsed("--workload", "decode", "--seed", "7")
+    assert w.seed == 7 and w.name.endswith("_seed7") and w.T == bench.workload("decode").T
+    with pytest.raises(SystemExit):
+        parsed("--T", "64")                                           # --T goes with padded only
