@@ -44,9 +44,9 @@
  *  R6 y = x / sqrt(mean(x^2) + eps) * (gamma + weight_bias);
  *  R7 MXFP8 block exponent: the smallest e with amax <= 448 * 2^e, stored as
  *     clamp(e + 127, 0, 254); amax == 0 stores 0;
- *  R9 NVFP4 block scale s = e4m3(amax(g*y) / 6); each element is scaled by
- *     the block scale's fp32 reciprocal, q = e2m1(fp32(g*y) * fp32(1/s)),
- *     q = 0 when s == 0; element 2i in the low nibble;
+ *  R9 NVFP4 block scale s = e4m3(amax(g*y) / 6); each element is divided
+ *     by the block scale, q = e2m1(fp32(fp32(g*y) / s)), q = 0 when s == 0;
+ *     element 2i in the low nibble;
  *  R10 the 128x4 swizzled scale layout of the cuBLAS block-scaling format;
  *  R16 MXFP4 block exponent: the smallest e with amax <= 6 * 2^e, like R7;
  *     fp16 I/O and bf16 / fp16 router weights decode exactly to fp64;
@@ -445,12 +445,11 @@ static void quant_nvfp4_row(const float *y32, int32_t H, int64_t t, int32_t layo
         uint8_t sc = oracle_e4m3_from_f64((double)sdiv);
         double s = oracle_e4m3_to_f64(sc);
         scales[oracle_sf_offset(t, c, C, layout)] = sc;
-        float rs = (s != 0.0) ? (float)(1.0 / s) : 0.0f; /* fp32 reciprocal of the scale */
         for (int i = 0; i < 16; i += 2) {
             uint8_t lo = 0, hi = 0;
-            if (s != 0.0) {
-                lo = oracle_e2m1_from_f64((double)(float)((double)v[i] * (double)rs));
-                hi = oracle_e2m1_from_f64((double)(float)((double)v[i + 1] * (double)rs));
+            if (s != 0.0) {                               /* fp32 quotients v / s */
+                lo = oracle_e2m1_from_f64((double)(float)((double)v[i] / s));
+                hi = oracle_e2m1_from_f64((double)(float)((double)v[i + 1] / s));
             }
             q[c * 8 + i / 2] = (uint8_t)(lo | (hi << 4));
         }

@@ -78,6 +78,66 @@ def test_worked_example_golden():
     assert o4["quant"][1].tolist() == [int(v, 16) for v in ex["nvfp4_bytes_t1"]]
 
 
+def _nvfp4_midpoint_golden():
+    return json.load(open(os.path.join(HERE, "golden", "nvfp4_midpoints.json")))
+
+
+def _e2m1_rne_f32_codes(x):
+    """e2m1 codes of float values by nearest-value search over the grid,
+    ties to the even code, saturating at 6 (written out here, not taken from
+    the oracle)."""
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float64)
+    out = []
+    for v in np.asarray(x, np.float64):
+        a = min(abs(v), 6.0)
+        dist = np.abs(grid - a)
+        best = np.flatnonzero(dist == dist.min())
+        c = int(best[0]) if best.size == 1 else int(best[best % 2 == 0][0])
+        out.append(c | (8 if v < 0 and c else 0))
+    return out
+
+
+def test_nvfp4_midpoint_golden_divides_by_the_block_scale():
+    # elements exactly on e2m1 midpoints once divided by the block scale; the
+    # expected bytes are hand-derived in the fixture
+    g = _nvfp4_midpoint_golden()
+    H = g["H"]
+    row = bf(np.array(g["row"], np.float64))[None, :]
+    assert np.array_equal(f(row)[0], g["row"])           # the row is exact in bf16
+    o = oracle.combine(row, np.zeros((1, 1), np.int32), np.ones((1, 1), np.float32), quant="nvfp4",
+                       global_scale=g["global_scale"], outputs=("quant",))
+    assert o["status"] == 0
+    assert o["scales"].tolist() == [int(v, 16) for v in g["expect"]["scales"]]
+    assert o["quant"][0].tolist() == [int(v, 16) for v in g["expect"]["bytes"]]
+    # the global scale acts before the block scaling: a row 4x smaller with
+    # g = 4 gives the same bytes
+    o4 = oracle.combine(bf(np.array(g["row"]) / 4)[None, :], np.zeros((1, 1), np.int32),
+                        np.ones((1, 1), np.float32), quant="nvfp4", global_scale=4.0, outputs=("quant",))
+    assert o4["quant"].tolist() == o["quant"].tolist() and o4["scales"].tolist() == o["scales"].tolist()
+    assert H == 32
+
+
+def test_nvfp4_midpoint_golden_separates_the_reciprocal_reading():
+    # the other plausible reading, an element times the fp32 reciprocal of its
+    # block scale, written out in float32 arithmetic: it must give the
+    # fixture's other bytes, so the golden above cannot pass under it
+    g = _nvfp4_midpoint_golden()
+    v = np.array(g["row"], np.float32)
+    scales = [1.875, 0.234375]
+    codes = []
+    for b in range(2):
+        rs = np.float32(1.0) / np.float32(scales[b])
+        codes += _e2m1_rne_f32_codes((v[16 * b:16 * b + 16] * rs).astype(np.float32))
+        # and the quotient reading, for the expected bytes
+    packed = [codes[2 * i] | (codes[2 * i + 1] << 4) for i in range(16)]
+    assert packed == [int(x, 16) for x in g["expect"]["bytes_if_reciprocal"]]
+    assert packed != [int(x, 16) for x in g["expect"]["bytes"]]
+    qcodes = []
+    for b in range(2):
+        qcodes += _e2m1_rne_f32_codes(np.array(g["row"][16 * b:16 * b + 16]) / scales[b])
+    assert [qcodes[2 * i] | (qcodes[2 * i + 1] << 4) for i in range(16)] == [int(x, 16) for x in g["expect"]["bytes"]]
+
+
 # -------------------------------------------------------------- the sum ---
 
 def test_top1_unit_weight_is_a_pure_gather():
