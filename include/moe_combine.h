@@ -81,7 +81,9 @@ typedef enum {
     MOE_QUANT_NONE = 0,
     MOE_QUANT_MXFP8 = 1, /* e4m3 codes [T, H] bytes + UE8M0 scale per 32 elements */
     MOE_QUANT_NVFP4 = 2, /* e2m1 codes [T, H/2] bytes (element 2i in the low nibble)
-                            + e4m3 scale per 16 elements, with global scale g */
+                            + e4m3 scale s = e4m3(amax(g * y) / 6) per 16 elements,
+                            with global scale g; code = e2m1 of the quotient
+                            (g * y) / s, correctly rounded to fp32 */
     MOE_QUANT_MXFP4 = 3  /* e2m1 codes [T, H/2] bytes (element 2i in the low nibble)
                             + UE8M0 scale per 32 elements: the smallest e with
                             amax <= 6 * 2^e, biased by 127 (global_scale ignored) */
@@ -197,9 +199,12 @@ moe_status moe_build_row_map_launches(int64_t T, int32_t top_k, int32_t E, int32
  *  - Limit: moe_build_row_map_workspace_size(T, top_k, E) must not exceed
  *    MOE_NOALLOC_SCRATCH_BYTES (1 MiB: for example T * top_k up to about one
  *    million slots with E = 256); larger problems return MOE_ERR_UNSUPPORTED.
- *  - The first call on each device looks up the array's device address
- *    (once per device, with that device current); make that first call
- *    before any stream capture.
+ *  - The first call in each CUDA context looks up the array's device
+ *    address there (cudaGetSymbolAddress, with that device current) and
+ *    remembers it under the context's id; make that first call before any
+ *    stream capture.  A context created later on the same device (after
+ *    cudaDeviceReset, or a caller's own driver-API context) gets its own
+ *    lookup on its first call.
  *  - All calls on a device share the one array, and it keeps whatever the
  *    last call left in it; every call rewrites the parts it reads.  Calls
  *    that may overlap on the GPU (different streams, or host threads) race

@@ -13,7 +13,7 @@
 //   MXFP8: per 32 elements, e = smallest integer with amax <= 448 * 2^e,
 //          byte = clamp(e + 127, 0, 254), code = e4m3_rn_sat(y * 2^-e)
 //   NVFP4: v = g * y; per 16 elements s = e4m3_rn_sat(amax(v) / 6),
-//          code = e2m1_rn_sat(v * rn(1 / s)) (0 when s == 0)
+//          code = e2m1_rn_sat(rn(v / s)) (0 when s == 0)
 //   MXFP4: per 32 elements, e = smallest integer with amax <= 6 * 2^e,
 //          byte = clamp(e + 127, 0, 254), code = e2m1_rn_sat(y * 2^-e)
 // Inputs and outputs are bf16 or fp16 (io_dtype); router weights fp32,

@@ -72,7 +72,7 @@ struct SmemLayout {
 // barrier, and the two cross-CTA reduction barriers of a split
 // token), the slots' StageMeta, two buffers of per-warp partial sums for
 // csize CTAs, then (with a norm) the Hl gamma values, then a table of the
-// reciprocals of the e4m3 block scales (NVFP4).
+// e4m3 block scales' values and reciprocals (NVFP4).
 __host__ __device__ inline SmemLayout smem_layout(int32_t Hl, int32_t stages, int32_t rows, int32_t ncw,
                                                   int32_t csize, bool with_gamma)
 {
@@ -84,7 +84,7 @@ __host__ __device__ inline SmemLayout smem_layout(int32_t Hl, int32_t stages, in
     L.red = L.meta + static_cast<uint32_t>(stages) * static_cast<uint32_t>(sizeof(StageMeta));
     L.gamma = (L.red + 2u * static_cast<uint32_t>(csize) * static_cast<uint32_t>(ncw) * 4u + 127u) & ~127u;
     L.rtab = (L.gamma + (with_gamma ? static_cast<uint32_t>(Hl) * 2u : 0u) + 15u) & ~15u;
-    L.total = L.rtab + 128u * 4u;  // the reciprocals of the 128 non-negative e4m3 codes
+    L.total = L.rtab + 128u * 8u;  // value and reciprocal of the 128 non-negative e4m3 codes
     return L;
 }
 
@@ -270,11 +270,11 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
         fence_mbar_init();
     }
     if constexpr (QUANT == MOE_QUANT_NVFP4) {
-        // the correctly rounded fp32 reciprocal of every non-negative e4m3
-        // code's value (0 for code 0, which is never divided by)
-        float *rtab = reinterpret_cast<float *>(smem + L.rtab);
+        // every non-negative e4m3 code's value and its correctly rounded fp32
+        // reciprocal (0 for code 0, which is never divided by)
+        float2 *rtab = reinterpret_cast<float2 *>(smem + L.rtab);
         for (uint32_t c = threadIdx.x; c < 128u; c += blockDim.x)
-            rtab[c] = c ? __frcp_rn(e4m3_code_value(c)) : 0.f;
+            rtab[c] = make_float2(e4m3_code_value(c), c ? __frcp_rn(e4m3_code_value(c)) : 0.f);
     }
     // with SPLIT, every CTA's barriers are initialised before any peer arrives on them
     if constexpr (SPLIT)
@@ -717,13 +717,14 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                         if (vv) {
                             uint32_t packed = 0;
                             if (sc != 0u) {
-                                // elements are scaled by the block scale's correctly
-                                // rounded fp32 reciprocal, from the table
-                                const float rs = reinterpret_cast<const float *>(smem + L.rtab)[sc];
+                                // each element divided by the block scale, the
+                                // quotient correctly rounded to fp32 (from the
+                                // scale's value and reciprocal in the table)
+                                const float2 sr = reinterpret_cast<const float2 *>(smem + L.rtab)[sc];
                                 float qv[8];
 #pragma unroll
-                                for (int i = 0; i < 8; ++i)
-                                    qv[i] = g[i] * rs;
+                                for (int i = 0; i < 8; i += 2)
+                                    div_scale_rn2(g[i], g[i + 1], sr.x, sr.y, qv[i], qv[i + 1]);
                                 packed = cvt_e2m1x8(qv);
                             }
                             *reinterpret_cast<uint32_t *>(p.quant_out + (row0 >> 1) + 4 * v) = packed;

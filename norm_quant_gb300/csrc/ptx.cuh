@@ -231,6 +231,28 @@ __device__ __forceinline__ float div6_rn(float x)
     return __fmaf_rn(r, c, q);
 }
 
+// a0 / s and a1 / s rounded to nearest even, without a division, wherever
+// the quotient is a normal float, given rs = RN(1/s): the same FMA-corrected
+// product as div6_rn (Markstein's theorem), on two lanes at once with the
+// packed fp32 instructions.  q = RN(a * rs) is within one ulp of a / s, the
+// remainder a - q * s is exact in one fma, and RN(q + (a - q * s) * rs) is the
+// correctly rounded quotient.  The theorem assumes the remainder does not
+// underflow: for an element below 2^-100 it can, and the quotient may differ
+// in its last place, but it is then below 2^-91 and its e2m1 code 0 either
+// way.  Checked against the correctly rounded division for every positive
+// e4m3 block scale and every float a block with that scale can hold.
+__device__ __forceinline__ void div_scale_rn2(float a0, float a1, float s, float rs, float &q0, float &q1)
+{
+    uint64_t a, q, r, rr, ns;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(rr) : "f"(rs));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(ns) : "f"(-s));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q) : "l"(a), "l"(rr));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(q), "l"(ns), "l"(a));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(q) : "l"(r), "l"(rr));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(q0), "=f"(q1) : "l"(q));
+}
+
 // ------------------------------------------------------------ conversions
 
 // Two fp32 -> two e4m3 (round to nearest even, saturate to +-448); `lo`
