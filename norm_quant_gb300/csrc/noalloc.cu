@@ -1,7 +1,9 @@
 // noalloc.cu -- the routing build for callers that cannot allocate device
 // memory: its scratch lives in a fixed array that the library itself holds.
-#include <atomic>
 #include <cstdint>
+#include <mutex>
+
+#include <cuda.h>  // CUcontext and CUresult types only; no libcuda symbol is linked
 #include <cuda_runtime.h>
 
 #include "common.h"
@@ -14,21 +16,67 @@ namespace {
 // comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_route_scratch[MOE_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_route_scratch on the current device, looked up once per
-// device (with that device current); nullptr if the lookup fails.
+// The current CUDA context's process-unique id (cuCtxGetId), or 0 when no
+// context is current or the driver cannot say.  The driver functions come
+// through the runtime's entry-point query, so the library links no libcuda.
+unsigned long long current_context_id()
+{
+    using get_current_fn = CUresult (*)(CUcontext *);
+    using get_id_fn = CUresult (*)(CUcontext, unsigned long long *);
+    static get_current_fn get_current = nullptr;
+    static get_id_fn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<get_current_fn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<get_id_fn>(f);
+        cudaGetLastError();
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_route_scratch in the current context, looked up with
+// cudaGetSymbolAddress the first time a context asks and remembered under the
+// context's id: a context made after cudaDeviceReset, or a caller's own
+// driver-API context, gets its own lookup instead of an address that belongs
+// to another context.  nullptr if the lookup fails.
 void *route_scratch_address()
 {
-    static std::atomic<void *> addr[64];  // static storage: starts null
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    struct Entry {
+        unsigned long long ctx;
+        void *addr;
+    };
+    static Entry cache[64];  // static storage: starts empty
+    static int used = 0;
+    static std::mutex mu;
+    unsigned long long id = current_context_id();
+    if (id) {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i)
+            if (cache[i].ctx == id)
+                return cache[i].addr;
+    }
+    void *a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_route_scratch) != cudaSuccess) {
+        cudaGetLastError();
         return nullptr;
-    void *a = addr[dev].load(std::memory_order_acquire);
-    if (!a) {
-        if (cudaGetSymbolAddress(&a, g_route_scratch) != cudaSuccess) {
-            cudaGetLastError();
-            return nullptr;
-        }
-        addr[dev].store(a, std::memory_order_release);  // every thread finds the same address
+    }
+    if (!id)
+        id = current_context_id();  // the lookup made the device's primary context current
+    if (id) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (used < 64)
+            cache[used++] = Entry{id, a};  // a full table only means later lookups repeat
     }
     return a;
 }
