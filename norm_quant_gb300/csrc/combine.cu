@@ -175,6 +175,7 @@ extern "C" moe_status moe_combine(const moe_combine_args *a, moe_stream_t stream
     p.residual = static_cast<const uint8_t *>(a->residual);
     p.gamma = static_cast<const uint16_t *>(a->gamma);
     p.eps = a->eps;
+    p.inv_h = 1.0f / static_cast<float>(a->H);
     p.wb = a->weight_bias;
     p.gscale = a->global_scale;
     p.sf_layout = a->sf_layout;

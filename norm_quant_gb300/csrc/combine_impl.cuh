@@ -50,6 +50,7 @@ struct Params {
     const uint8_t *residual;
     const uint16_t *gamma;
     float eps, wb, gscale;
+    float inv_h;           // 1 / H in fp32 (the mean of the squares is their sum times this)
     int32_t weight_dtype;  // moe_weight_dtype of router_weights
     int32_t sf_layout;
     uint16_t *combined_out, *residual_out, *norm_out;
@@ -276,11 +277,14 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
         for (uint32_t c = threadIdx.x; c < 128u; c += blockDim.x)
             rtab[c] = make_float2(e4m3_code_value(c), c ? __frcp_rn(e4m3_code_value(c)) : 0.f);
     }
-    // with SPLIT, every CTA's barriers are initialised before any peer arrives on them
+    __syncthreads();
+    // with SPLIT, every CTA's barriers are initialised before any peer arrives
+    // on them: each thread arrives on the cluster barrier here and waits on it
+    // only before its first access to a peer's shared memory (the norm's
+    // exchange), so the barrier's latency hides behind the rows' copies
+    bool cl_waited = !SPLIT, cl_arrived2 = !SPLIT;
     if constexpr (SPLIT)
-        cluster_arrive_wait();
-    else
-        __syncthreads();
+        cluster_arrive_rel();
     // launched as a programmatic dependent: nothing before this line touches
     // global memory, so the setup above overlaps the previous kernel's tail
     grid_dependency_wait();
@@ -585,6 +589,10 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                         // that has not yet read its partials.
                         const uint32_t par = tok & 1u;
                         part = red + par * csize * static_cast<uint32_t>(ncw);
+                        if (!cl_waited) {
+                            cluster_wait_acq();
+                            cl_waited = true;
+                        }
                         __syncwarp();
                         if (static_cast<uint32_t>(lane) < csize) {
                             const uint32_t mine = smem_u32(part + crank * ncw + warp);
@@ -597,6 +605,14 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                             return;
                         }
                         np = static_cast<int>(csize) * ncw;
+                        if (t + nunits() >= p.T) {
+                            // the CTA's last exchange: every peer has written
+                            // into this CTA's shared memory for the last time
+                            // and this thread into theirs, so it arrives on the
+                            // exit barrier now and waits on it at the very end
+                            cluster_arrive_rel();
+                            cl_arrived2 = true;
+                        }
                     } else {
                         float *mine = red + (tok & 1u) * ncw;
                         if (lane == 0)
@@ -616,7 +632,7 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
 #pragma unroll
                     for (int d = 16; d > 0; d >>= 1)
                         total += __shfl_xor_sync(0xffffffffu, total, d);
-                    const float rinv = 1.0f / sqrtf(total / static_cast<float>(H) + p.eps);
+                    const float rinv = rsqrt_newton(fmaf(total, p.inv_h, p.eps));
 #pragma unroll
                     for (int s = 0; s < VPT; ++s) {
                         const uint32_t gv[4] = {gq[s].x, gq[s].y, gq[s].z, gq[s].w};
@@ -742,10 +758,16 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
         }();
     }
     // with SPLIT, no CTA leaves while a peer may still write into its shared
-    // memory or arrive on its barriers (every wait above is bounded, so every
-    // thread gets here)
-    if constexpr (SPLIT)
-        cluster_arrive_wait();
+    // memory or arrive on its barriers.  Every wait above is bounded, so every
+    // thread gets here; one that left its work early (a wait gave up, or the
+    // producer) completes its arrive-wait-arrive sequence here.
+    if constexpr (SPLIT) {
+        if (!cl_waited)
+            cluster_wait_acq();
+        if (!cl_arrived2)
+            cluster_arrive_rel();
+        cluster_wait_acq();
+    }
 }
 
 // ------------------------------------------------------------------- host

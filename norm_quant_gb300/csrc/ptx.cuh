@@ -127,6 +127,12 @@ __device__ __forceinline__ void cluster_arrive_wait()
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// The two halves of cluster_arrive_wait, for work placed between them: every
+// thread of the cluster must alternate arrive and wait, and a wait completes
+// once every thread of the cluster that has not exited has arrived.
+__device__ __forceinline__ void cluster_arrive_rel() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait_acq() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
 // Address of the same shared-memory location in cluster CTA `rank`.
 __device__ __forceinline__ uint32_t cluster_map(uint32_t local, uint32_t rank)
 {
@@ -251,6 +257,19 @@ __device__ __forceinline__ void div_scale_rn2(float a0, float a1, float s, float
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(q), "l"(ns), "l"(a));
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(q) : "l"(r), "l"(rr));
     asm("mov.b64 {%0, %1}, %2;" : "=f"(q0), "=f"(q1) : "l"(q));
+}
+
+// 1 / sqrt(m) for m > 0: the hardware's reciprocal square root (rsqrtf,
+// within 2 ulps) refined by one step of Newton's method for f(r) = 1/r^2 - m,
+// r' = r + r (1 - m r^2) / 2, which squares the relative error.  For m outside
+// the normal range (0, subnormal, infinity) it returns rsqrtf(m) unrefined, so
+// a zero sum of squares still gives infinity and an overflowed one 0.
+// Checked against the correctly rounded __frsqrt_rn on every normal float.
+__device__ __forceinline__ float rsqrt_newton(float m)
+{
+    const float r = rsqrtf(m);
+    const float refined = __fmaf_rn(0.5f * r, __fmaf_rn(-m, r * r, 1.0f), r);
+    return (m >= 0x1p-126f && m <= 0x1.fffffep127f) ? refined : r;
 }
 
 // ------------------------------------------------------------ conversions
