@@ -41,6 +41,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE combine tokens/s and achieved HBM GB/s vs peak (T=4096,H=7168,k=8)"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0   # GB300's HBM3e, NVIDIA's nominal figure (8 stacks)
 L2_FLUSH_BYTES = 256 << 20
 # every source the combine kernels are compiled from
 KERNEL_SOURCES = ["norm_quant_gb300/csrc/combine.cu", "norm_quant_gb300/csrc/combine_impl.cuh",
@@ -72,8 +73,9 @@ def parse():
                     help="with --workload padded: a point of its token-count sweep (seed 2000 + T)")
     ap.add_argument("--seed", type=int, default=None,
                     help="another seed for the workload's synthetic inputs (default: the workload's own)")
-    ap.add_argument("--l2", choices=["none", "write"], default="none",
-                    help="none: inputs larger than L2; write: 256 MB write before each step")
+    ap.add_argument("--l2", choices=["none", "write", "read"], default="none",
+                    help="none: inputs larger than L2; write: 256 MB write before each step (leaves L2 "
+                    "full of dirty lines); read: 256 MB read before each step (leaves it full of clean lines)")
     return ap.parse_args()
 
 
@@ -178,8 +180,9 @@ def kernel_hash(read=None) -> str:
 
 def recorded_traffic(kind="prefill", read=None):
     """DRAM bytes per combine launch from the workload's committed ncu
-    summary, or None if there is none or the kernel source changed since
-    those counters were taken."""
+    summary, with the summary's capture date and kernel source hash; None if
+    there is no summary or the kernel source changed since those counters
+    were taken."""
     read = read or (lambda f: open(os.path.join(ROOT, f)).read())
     if kind not in TRAFFIC_FILES:
         return None
@@ -189,9 +192,24 @@ def recorded_traffic(kind="prefill", read=None):
         return None
     m = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
     hsh = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    when = re.search(r"captured:\s*([0-9-]+)", text)
     if not m or not hsh or hsh.group(1) != kernel_hash():
         return None
-    return int(m.group(1))
+    return {"bytes": int(m.group(1)), "file": TRAFFIC_FILES[kind], "kernel_source_hash": hsh.group(1),
+            "captured": when.group(1) if when else None}
+
+
+def traffic_provenance(kind, traffic):
+    """Where roofline.traffic comes from (or why it is null)."""
+    if traffic:
+        return {"how": "dram__bytes_read.sum + dram__bytes_write.sum of one launch, from the committed ncu "
+                       "summary of this kernel source (not measured in this run)",
+                "file": traffic["file"], "kernel_source_hash": traffic["kernel_source_hash"],
+                "captured": traffic["captured"]}
+    if kind not in TRAFFIC_FILES:
+        return {"how": "null: no committed ncu summary for this workload"}
+    return {"how": "null: the committed ncu summary was taken on other kernel source (hash "
+                   f"{kernel_hash()} now), or the run flushes L2 between steps"}
 
 
 class ClockSampler:
@@ -429,7 +447,17 @@ def run_ours(args):
     names = [n for n in ("topk_ids", "weights", "expert_out", "shared", "residual", "gamma", "x")
              if inp.get(n) is not None]
     host = {n: pinned(inp[n]) for n in names}
-    flush = torch.empty(L2_FLUSH_BYTES if args.l2 == "write" else 16, dtype=torch.uint8, device=dev)
+    flush = torch.zeros(L2_FLUSH_BYTES if args.l2 != "none" else 16, dtype=torch.uint8, device=dev)
+    flush_sum = torch.zeros((), dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        """Evicts the step's data from L2: by writing 256 MB (the lines it
+        leaves are dirty and are written back during the next step) or by
+        reading it (the lines it leaves are clean)."""
+        if args.l2 == "write":
+            flush.zero_()
+        elif args.l2 == "read":
+            flush_sum.copy_(flush.view(torch.int64).max())
     stream = torch.cuda.current_stream(dev)
     route_kernels = 0 if kind == "slot_major" else nqg.moe_build_row_map_launches(T, k, E)
 
@@ -488,8 +516,7 @@ def run_ours(args):
     gs = torch.cuda.Stream(dev)
     with torch.cuda.stream(gs):
         for _ in range(3):  # first calls configure the kernels; outside capture
-            if args.l2 == "write":
-                flush.zero_()
+            flush_l2()
             step(gs.cuda_stream)
     torch.cuda.synchronize()
     if kind != "slot_major":
@@ -500,7 +527,7 @@ def run_ours(args):
     # flush before every step, one step per graph keeps the flush outside the
     # timed events
     K = args.steps
-    G = 1 if args.l2 == "write" else next(g for g in (10, 8, 5, 4, 2, 1) if K % g == 0)
+    G = 1 if args.l2 != "none" else next(g for g in (10, 8, 5, 4, 2, 1) if K % g == 0)
 
     def graph_of(fn, n):
         g = torch.cuda.CUDAGraph()
@@ -520,10 +547,10 @@ def run_ours(args):
         gives each replay's duration."""
         replay_s.clear()
         with torch.cuda.stream(gs):
-            if args.l2 == "write":
+            if args.l2 != "none":
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 for _ in range(n):
-                    flush.zero_()
+                    flush_l2()
                     e0.record(gs)
                     g.replay()
                     e1.record(gs)
@@ -607,6 +634,7 @@ def run_ours(args):
             byt = algorithmic_bytes(wl, inp["n_valid"], "slot_major" if kind == "slot_major" else "grouped")
         comb_avg_s = comb_s
         achieved = byt["total"] / comb_avg_s / 1e9
+        traffic = recorded_traffic(kind) if args.l2 == "none" else None
         peak, peak_kind = measured_peak()
         line = {
             "metric": METRIC, "value": job_throughput(world, T, K, total_s), "unit": "tokens/s", "n_gpus": world,
@@ -619,8 +647,9 @@ def run_ours(args):
                               f"out: {'+'.join(wl.outputs)}"
                               + (f" ({wl.quant}, {wl.sf_layout} scales)" if wl.quant else "")
                               + (", slot-major [k, T, H] expert rows" if kind == "slot_major" else "")),
-                       "l2": ("256 MB L2 write-flush before each step, outside the timed events"
-                              if args.l2 == "write" else
+                       "l2": ({"write": "256 MB L2 write-flush before each step, outside the timed events",
+                               "read": "256 MB L2 read-flush before each step, outside the timed events"}
+                              .get(args.l2) or
                               f"no flush: each step streams {byt['total'] / 1e6:.0f} MB through the 129 MB L2"),
                        "timing": f"K steps (routing build + combine) as K/{G} replays of a CUDA graph of "
                                  f"{G} consecutive steps, between two events; the roofline times the same "
@@ -630,10 +659,12 @@ def run_ours(args):
             "achieved_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
+                         "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                          "kernel": "dispatch_kernel" if kind == "dispatch" else "combine_kernel",
                          "kernel_ms": comb_avg_s * 1e3,
                          "algorithmic_bytes": byt["total"],
-                         "traffic": recorded_traffic(kind)},
+                         "traffic": traffic["bytes"] if traffic else None,
+                         "traffic_source": traffic_provenance(kind, traffic)},
             "e2e": {"value": job_throughput(world, T, args.e2e_steps, e2e_s), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": (route_kernels + 1) * K,
