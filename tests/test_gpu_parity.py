@@ -630,3 +630,55 @@ def test_nvfp4_midpoint_golden_exact_on_gpu():
     assert int(status.item()) == 0
     assert h(sc).tolist() == [int(v, 16) for v in g["expect"]["scales"]]
     assert h(q).tolist() == [int(v, 16) for v in g["expect"]["bytes"]]
+
+
+# ------------------------------------- exact sums: quantisers bit for bit --
+
+def _exact_sum_inputs(T, H, k, E, seed, shared=True):
+    """Inputs whose weighted sums are exact in fp32 whatever the order: rows of
+    6-bit integers times 2^-6..2^2 (exact in bf16), weights 2^-0..2^-3.  The
+    kernel then quantises exactly the oracle's value, so every code and scale
+    byte must agree; integer-valued data also puts many elements exactly on
+    rounding midpoints of the e4m3 and e2m1 grids."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    ids[rng.random((T, k)) < 0.05] = -1
+    ost, oc, oo, orm, osr = oracle.build_row_map(ids, E)
+    nv = int(oo[E])
+
+    def vals(shape):
+        m = rng.integers(-48, 49, shape).astype(np.float64)
+        e = rng.integers(-6, 3, shape[:-1] + (1,)).astype(np.float64)   # one exponent per row
+        return synth.f32_to_bf16_bits((m * 2.0 ** e).astype(np.float32))
+
+    inp = {"topk_ids": ids, "n_valid": nv, "expert_out": vals((nv, H)),
+           "weights": (2.0 ** -rng.integers(0, 4, (T, k))).astype(np.float32),
+           "shared": vals((T, H)) if shared else None, "residual": vals((T, H)), "gamma": None}
+    return inp, orm
+
+
+@pytest.mark.parametrize("quant,layout", [("mxfp8", "linear"), ("mxfp8", "swizzled"), ("nvfp4", "linear"),
+                                          ("nvfp4", "swizzled"), ("mxfp4", "linear")])
+def test_quantisers_bit_exact_on_exact_sums(quant, layout):
+    T, H, k, E = 301, 512, 8, 32
+    inp, orm = _exact_sum_inputs(T, H, k, E, seed=11 + len(quant) + len(layout))
+    wl = synth.Workload(name=f"exact_{quant}_{layout}", T=T, H=H, E=E, k=k, shared_std=1.0, residual=True,
+                        quant=quant, sf_layout=layout, outputs=("combined", "residual", "quant"))
+    g = 1.0   # NVFP4's global scale: a power of two keeps g * y exact (other g: the workload tests)
+    got = gpu_combine(wl, inp, d(orm), global_scale=g, canary=True)
+    assert got["status"] == 0
+    o = oracle_combine(wl, inp, orm, global_scale=g)
+    assert np.array_equal(got["combined"], o["combined"])
+    assert np.array_equal(got["residual"], o["residual"])
+    assert np.array_equal(got["scales"], o["scales"]), "scale bytes"
+    assert np.array_equal(got["quant"], o["quant"]), f"{int((got['quant'] != o['quant']).sum())} code bytes differ"
+    if quant == "nvfp4":
+        # the data reaches the case the element quotient exists for: elements
+        # exactly on an e2m1 midpoint of their block scale
+        y = oracle.combine(inp["expert_out"], orm, inp["weights"], shared=inp["shared"],
+                           residual=inp["residual"], outputs=("y",))["y"]
+        v = (np.float32(g) * y.astype(np.float32)).astype(np.float64).reshape(T, H // 16, 16)
+        s = oracle.e4m3_to_f64(o["scales"][oracle.sf_offsets(T, H // 16, layout)])[:, :, None]
+        mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+        on_mid = np.any(np.abs(v)[..., None] == mids * s[..., None], axis=-1)
+        assert on_mid.sum() > 50, on_mid.sum()
