@@ -543,22 +543,29 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
 
                 // -------------------------------------------------- epilogue
                 const int64_t row0 = t * H + col0;  // element offset of this CTA's slice of row t
-                if (p.combined_out && !combined_done) {
+                auto store_sums = [&]() {
+                    if (p.combined_out && !combined_done) {
 #pragma unroll
-                    for (int s = 0; s < VPT; ++s) {
-                        const int v = s * NC + tid;
-                        if (v < nvec)
-                            store16x8<IO>(p.combined_out, row0 + 8 * v, acc[s]);
+                        for (int s = 0; s < VPT; ++s) {
+                            const int v = s * NC + tid;
+                            if (v < nvec)
+                                store16x8<IO>(p.combined_out, row0 + 8 * v, acc[s]);
+                        }
                     }
-                }
-                if (p.residual_out) {
+                    if (p.residual_out) {
 #pragma unroll
-                    for (int s = 0; s < VPT; ++s) {
-                        const int v = s * NC + tid;
-                        if (v < nvec)
-                            store16x8<IO>(p.residual_out, row0 + 8 * v, acc[s]);
+                        for (int s = 0; s < VPT; ++s) {
+                            const int v = s * NC + tid;
+                            if (v < nvec)
+                                store16x8<IO>(p.residual_out, row0 + 8 * v, acc[s]);
+                        }
                     }
-                }
+                };
+                // with SPLIT and a norm, the sums are stored after this thread's
+                // release operations toward the peers (below), so that those
+                // do not wait for the stores to drain
+                if (!(SPLIT && do_norm))
+                    store_sums();
                 if (do_norm) {
                     uint4 gq[VPT];
 #pragma unroll
@@ -599,20 +606,23 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                             st_cluster_f32(cluster_map(mine, lane), ss);
                             mbar_arrive_cluster(cluster_map(xbar0 + 8u * par, lane));
                         }
+                        if (t + nunits() >= p.T) {
+                            // the CTA's last exchange: this thread has written
+                            // into its peers' shared memory for the last time,
+                            // so it arrives on the exit barrier now and waits on
+                            // it at the very end.  The barrier completes only
+                            // once every peer has arrived too, which each does
+                            // after its own last writes into this CTA.
+                            cluster_arrive_rel();
+                            cl_arrived2 = true;
+                        }
+                        store_sums();
                         if (__any_sync(0xffffffffu,
                                        !mbar_wait_cluster_bounded(xbar0 + 8u * par, (tok >> 1) & 1u, kWaitLimitNs))) {
                             report(p.status, MOE_ERR_DEVICE_TIMEOUT);
                             return;
                         }
                         np = static_cast<int>(csize) * ncw;
-                        if (t + nunits() >= p.T) {
-                            // the CTA's last exchange: every peer has written
-                            // into this CTA's shared memory for the last time
-                            // and this thread into theirs, so it arrives on the
-                            // exit barrier now and waits on it at the very end
-                            cluster_arrive_rel();
-                            cl_arrived2 = true;
-                        }
                     } else {
                         float *mine = red + (tok & 1u) * ncw;
                         if (lane == 0)
