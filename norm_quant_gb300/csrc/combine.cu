@@ -39,14 +39,18 @@
 //     slot on its "empty" mbarrier;
 //   * after a token's last slot: bf16 stores, a sum of squares reduced by
 //     warp shuffles and a cross-warp sum at a named barrier of the
-//     consumer warps, the norm,
-//     and the block quantiser (an MXFP8 block is 4 consecutive lanes, NVFP4 2);
+//     consumer warps, the norm (its scale 1 / sqrt(mean + eps) from rsqrt
+//     refined by one Newton step, within one ulp of the correctly rounded
+//     value), and the block quantiser (an MXFP8 block is 4 consecutive lanes,
+//     NVFP4 2; NVFP4 elements divided by their block scale, the quotient
+//     correctly rounded);
 //   * on request (moe_tuning_set), a token is split by columns over a
 //     thread-block cluster of 2..16 CTAs (each copies, sums, normalises and
 //     quantises its own slice of every row); the slices' sums of squares
 //     meet through distributed shared memory: each warp stores its partial
-//     into every CTA of the cluster and arrives on that CTA's mbarrier, and
-//     each CTA adds the partials in one fixed order;
+//     into every CTA of the cluster and arrives on that CTA's mbarrier (before
+//     the token's own global stores, which those release operations would
+//     otherwise wait for), and each CTA adds the partials in one fixed order;
 //   * gamma's slice is copied to shared memory once per CTA, and the
 //     per-warp partial sums of squares are added by a butterfly that gives
 //     every lane the same total.
