@@ -293,12 +293,14 @@ moe_status moe_combine(const moe_combine_args *args, moe_stream_t stream);
  *                  1..16 the largest thread-block cluster its single-launch
  *                  path may use;
  *   combine_split  CTAs that share one token's row, as a thread-block
- *                  cluster that splits the columns: 0 automatic (whole
- *                  rows, the faster choice measured at every T), 1 never,
- *                  2, 4, 8 or 16 always where H allows it (slices of equal
- *                  width holding whole quant blocks, at most 4096 columns
- *                  each; otherwise whole rows).  vpt, rows_per_slot and
- *                  ctas_per_sm apply to whole rows only.
+ *                  cluster that splits the columns: 0 automatic (4 CTAs a
+ *                  token while T * 4 <= the SM count and H >= 7168; with a
+ *                  quantised output 2 while T * 2 <= the SM count and
+ *                  H >= 7168; whole rows otherwise), 1 never, 2, 4, 8 or 16
+ *                  always where H allows it (slices of equal width holding
+ *                  whole quant blocks, at most 4096 columns each; otherwise
+ *                  whole rows).  vpt, rows_per_slot and ctas_per_sm apply
+ *                  to whole rows only.
  * Not synchronised with calls in flight on other host threads.  Returns
  * MOE_OK or MOE_ERR_INVALID_ARG.  (No counterpart on the pages: a tuning
  * hook of this implementation.) */

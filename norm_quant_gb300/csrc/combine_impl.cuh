@@ -265,8 +265,10 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
         }
         mbar_init(gbar, 1);
         if constexpr (SPLIT) {
-            mbar_init(xbar0, csize * ncw);
-            mbar_init(xbar0 + 8u, csize * ncw);
+            // one local arrival a token (with the expected bytes); the peers'
+            // partials complete the transaction bytes
+            mbar_init(xbar0, 1);
+            mbar_init(xbar0 + 8u, 1);
         }
         fence_mbar_init();
     }
@@ -415,12 +417,39 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
         // ----------------------------------------------------------- consumers
         [&]() {
             const int tid = threadIdx.x;
-            // pad rows of a swizzled scale matrix are written as zero
+            // pad rows of a swizzled scale matrix are written as zero.  They
+            // are rows T % 128 .. 127 of the last 128-row tile.  In that
+            // layout the 512 bytes of one column group of a tile hold, at
+            // 16 * L, the 4 columns of rows L, L + 32, L + 64 and L + 96: a
+            // warp clears a column group with lane L storing its 16 bytes, or
+            // only the 4-byte cells of pad rows where the lane holds real rows
             if (QUANT != MOE_QUANT_NONE && p.sf_layout == MOE_SF_SWIZZLED_128x4 && p.sf_rows_pad > p.T) {
-                const int64_t nz = (p.sf_rows_pad - p.T) * p.sf_cols_pad;
-                for (int64_t i = static_cast<int64_t>(blockIdx.x) * NC + tid; i < nz;
-                     i += static_cast<int64_t>(gridDim.x) * NC)
-                    p.scales_out[sf_offset(p.T + i / p.sf_cols_pad, i % p.sf_cols_pad, p)] = 0;
+                const uint32_t groups = static_cast<uint32_t>(p.sf_cols_pad >> 2);
+                const uint32_t r0 = static_cast<uint32_t>(p.T & 127);
+                uint8_t *const tile = p.scales_out + (p.T >> 7) * static_cast<int64_t>(groups) * 512;
+                const uintptr_t base = reinterpret_cast<uintptr_t>(p.scales_out);
+                const bool v16 = (base & 15u) == 0, w4 = (base & 3u) == 0;
+                for (uint32_t g = blockIdx.x * static_cast<uint32_t>(ncw) + warp; g < groups;
+                     g += gridDim.x * static_cast<uint32_t>(ncw)) {
+                    uint8_t *const cell = tile + g * 512u + static_cast<uint32_t>(lane) * 16u;
+                    if (static_cast<uint32_t>(lane) >= r0 && v16) {
+                        *reinterpret_cast<uint4 *>(cell) = make_uint4(0u, 0u, 0u, 0u);
+                        continue;
+                    }
+#pragma unroll
+                    for (uint32_t q = 0; q < 4; ++q) {
+                        if (static_cast<uint32_t>(lane) + 32u * q < r0)
+                            continue;  // a real row: its scales are the epilogue's
+                        if (w4) {
+                            *reinterpret_cast<uint32_t *>(cell + 4u * q) = 0u;
+                        } else {
+                            cell[4u * q] = 0;
+                            cell[4u * q + 1] = 0;
+                            cell[4u * q + 2] = 0;
+                            cell[4u * q + 3] = 0;
+                        }
+                    }
+                }
             }
             const bool do_norm = p.gamma != nullptr;
             const int max_slots = k + 3;  // a token never needs more slots than rows + 1
@@ -600,11 +629,16 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                             cluster_wait_acq();
                             cl_waited = true;
                         }
+                        // this token's partials from every warp of every CTA
+                        // arrive as transaction bytes (the count can run below
+                        // zero before this arrival sets it, and the phase still
+                        // waits for the arrival)
+                        if (warp == 0 && lane == 0)
+                            mbar_arrive_expect_tx(xbar0 + 8u * par, csize * static_cast<uint32_t>(ncw) * 4u);
                         __syncwarp();
                         if (static_cast<uint32_t>(lane) < csize) {
                             const uint32_t mine = smem_u32(part + crank * ncw + warp);
-                            st_cluster_f32(cluster_map(mine, lane), ss);
-                            mbar_arrive_cluster(cluster_map(xbar0 + 8u * par, lane));
+                            st_async_cluster_f32(cluster_map(mine, lane), ss, cluster_map(xbar0 + 8u * par, lane));
                         }
                         if (t + nunits() >= p.T) {
                             // the CTA's last exchange: this thread has written
@@ -806,16 +840,31 @@ inline bool split_ok(int32_t H, int32_t quant, int c)
     return c >= 2 && c <= kMaxSplit && H % (c * blk) == 0 && H / c <= kMaxSplitCols;
 }
 
-// CTAs per token: 1 unless moe_tuning_set asks for a cluster size.  Measured
-// on GB300 (graphs of back-to-back launches, H = 7168, k = 8, T = 1..128),
-// splitting never paid: the combine at decode sizes is bound by a fixed chain
-// of latencies (launch, row_map load, row copies, epilogue), not by one SM's
-// share of HBM bandwidth, and a cluster adds its own launch and barrier cost
-// (T = 64: 5.7 us whole rows, 6.4 us in pairs, 10.1 us in clusters of 16).
-inline int choose_split(int32_t H, int64_t, int32_t quant, int forced)
+// CTAs per token.  moe_tuning_set may ask for a cluster size (or 1, whole
+// rows); otherwise small batches split their rows over a thread-block cluster
+// while every CTA of it finds an SM of its own and keeps a slice of at least
+// 1792 columns: 4 CTAs a token up to sms / 4 tokens, and, with a quantised
+// output, 2 up to sms / 2 tokens; whole rows otherwise.  Measured on GB300
+// (graphs of 50 launches, k = 8, E = 256 / 128):
+//   H = 7168, residual + norm, bf16 out: T = 1: 4.28 us whole, 3.85 in 4s;
+//     T = 38: 4.43, 4.20 in 4s; T = 64: 4.46 whole, 4.58 in pairs;
+//   H = 7168, shared + residual + norm + MXFP8: T = 1: 5.42, 4.18 in 4s;
+//     T = 64: 5.62, 4.96 in pairs; T = 100: 5.74 whole, 9.40 in pairs;
+//   H = 4096, NVFP4: slower split from T = 32 (T = 64: 4.28 whole, 4.65 pairs).
+// A split token's CTAs each stage and sum a slice of every row, which halves
+// or quarters one SM's copy intake and consumer work; the slices' sums of
+// squares cost one exchange through distributed shared memory.
+inline int choose_split(int32_t H, int64_t T, int32_t quant, int forced)
 {
     if (forced >= 2)
         return split_ok(H, quant, forced) ? forced : 1;
+    if (forced == 1)
+        return 1;
+    const int64_t sms = sm_count();
+    if (T * 4 <= sms && H / 4 >= 1792 && split_ok(H, quant, 4))
+        return 4;
+    if (quant != MOE_QUANT_NONE && T * 2 <= sms && H / 2 >= 3584 && split_ok(H, quant, 2))
+        return 2;
     return 1;
 }
 

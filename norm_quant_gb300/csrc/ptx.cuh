@@ -146,6 +146,17 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t remote, float v)
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
+// An asynchronous store of one float into another CTA's shared memory whose
+// completion counts 4 transaction bytes on an mbarrier of that CTA (both
+// addresses from cluster_map): the data is visible to a thread that has seen
+// the barrier's phase complete, and the storing thread does not wait.
+__device__ __forceinline__ void st_async_cluster_f32(uint32_t remote, float v, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(remote), "f"(v),
+                 "r"(remote_bar)
+                 : "memory");
+}
+
 // Arrives on an mbarrier of another CTA of the cluster, releasing this
 // thread's earlier memory operations at cluster scope.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar)

@@ -682,3 +682,38 @@ def test_quantisers_bit_exact_on_exact_sums(quant, layout):
         mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
         on_mid = np.any(np.abs(v)[..., None] == mids * s[..., None], axis=-1)
         assert on_mid.sum() > 50, on_mid.sum()
+
+
+# ----------------------------- swizzled scales: pad rows at any alignment --
+
+@pytest.mark.parametrize("offset", [0, 1, 4, 8])
+@pytest.mark.parametrize("quant,T", [("nvfp4", 1), ("nvfp4", 37), ("mxfp8", 5), ("mxfp8", 130)])
+def test_swizzled_scales_pad_rows_at_any_alignment(quant, T, offset):
+    # the scale buffer may start at any byte; its pad rows (T % 128 .. 127 of
+    # the last row tile) are zeroed with 16-byte, 4-byte or 1-byte stores as
+    # the start allows, and no byte outside the buffer is touched
+    H = 208 if quant == "nvfp4" else 224   # 13 or 7 scale columns, padded to 16 / 8
+    wl = synth.Workload(name=f"swz_{quant}_{T}_{offset}", T=T, H=H, E=8, k=2, residual=True,
+                        quant=quant, sf_layout="swizzled", outputs=("residual", "quant"), seed=T + offset)
+    inp = synth.make_inputs(wl)
+    d_rm, orm = route_and_check(inp["topk_ids"], wl.E)
+    g = nvfp4_global_scale(wl, inp, orm) if quant == "nvfp4" else 1.0
+    n = nqg.moe_scales_bytes(T, H, quant, "swizzled")
+    buf = torch.full((n + 64,), 0x5A, dtype=torch.uint8, device="cuda")
+    scales = buf[offset:offset + n]
+    q = torch.empty((T, H if quant == "mxfp8" else H // 2), dtype=torch.uint8, device="cuda")
+    res = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nqg.moe_combine(expert_out=d(inp["expert_out"]), row_map=d_rm, router_weights=d(inp["weights"]),
+                    residual=d(inp["residual"]), quant=quant, sf_layout="swizzled", global_scale=g,
+                    residual_out=res, quant_out=q, scales_out=scales, status=status, H=H)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    o = oracle_combine(wl, inp, orm, global_scale=g)
+    b = h(buf)
+    assert np.all(b[:offset] == 0x5A) and np.all(b[offset + n:] == 0x5A), "bytes outside the scale buffer"
+    got = b[offset:offset + n]
+    used = np.zeros(n, bool)
+    used[oracle.sf_offsets(T, H // (16 if quant == "nvfp4" else 32), "swizzled").ravel()] = True
+    assert np.all(got[~used] == 0), "pad bytes not zero"
+    assert_quant_close(wl, h(q), got, o["quant"], o["scales"], T, H, g, wl.name)
