@@ -44,13 +44,15 @@
 //     value), and the block quantiser (an MXFP8 block is 4 consecutive lanes,
 //     NVFP4 2; NVFP4 elements divided by their block scale, the quotient
 //     correctly rounded);
-//   * on request (moe_tuning_set), a token is split by columns over a
-//     thread-block cluster of 2..16 CTAs (each copies, sums, normalises and
-//     quantises its own slice of every row); the slices' sums of squares
-//     meet through distributed shared memory: each warp stores its partial
-//     into every CTA of the cluster and arrives on that CTA's mbarrier (before
-//     the token's own global stores, which those release operations would
-//     otherwise wait for), and each CTA adds the partials in one fixed order;
+//   * for small batches, or on request (moe_tuning_set), a token is split by
+//     columns over a thread-block cluster of 2..16 CTAs (each copies, sums,
+//     normalises and quantises its own slice of every row); the slices' sums of squares
+//     meet through distributed shared memory: each warp sends its partial to
+//     every CTA of the cluster as an asynchronous store that completes on that
+//     CTA's mbarrier, and each CTA adds the partials in one fixed order.  This
+//     is the automatic plan for small batches (4 CTAs a token while T * 4 <=
+//     the SM count and H >= 7168; 2 for quantised output while T * 2 <= the
+//     SM count), where it halves or quarters one SM's copies and sums;
 //   * gamma's slice is copied to shared memory once per CTA, and the
 //     per-warp partial sums of squares are added by a butterfly that gives
 //     every lane the same total.

@@ -617,9 +617,10 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                     int32_t aborted = 0;
                     if constexpr (SPLIT) {
                         // every warp of every CTA of the cluster sends its partial
-                        // to slot [rank][warp] of every CTA (lane r to CTA r) and
-                        // arrives there; each CTA then adds all csize * ncw of
-                        // them in the same order, so the whole token sees one
+                        // to slot [rank][warp] of every CTA (lane r to CTA r) as
+                        // an asynchronous store that completes on that CTA's
+                        // exchange barrier; each CTA then adds all csize * ncw
+                        // of them in the same order, so the whole token sees one
                         // norm.  Buffers and barriers alternate with the token's
                         // parity: a CTA can run at most one token ahead of a peer
                         // that has not yet read its partials.
@@ -645,8 +646,10 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
                             // into its peers' shared memory for the last time,
                             // so it arrives on the exit barrier now and waits on
                             // it at the very end.  The barrier completes only
-                            // once every peer has arrived too, which each does
-                            // after its own last writes into this CTA.
+                            // once every peer has arrived too, each after its
+                            // own last stores into this CTA; the release orders
+                            // those stores before the arrival (a relaxed arrive,
+                            // measured faster, would not).
                             cluster_arrive_rel();
                             cl_arrived2 = true;
                         }

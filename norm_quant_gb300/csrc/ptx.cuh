@@ -120,16 +120,9 @@ __device__ __forceinline__ uint32_t cluster_count_x()
     return r;
 }
 
-// Every thread of the cluster that has not exited arrives (release) and
-// waits (acquire); usable from divergent code.
-__device__ __forceinline__ void cluster_arrive_wait()
-{
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
-// The two halves of cluster_arrive_wait, for work placed between them: every
-// thread of the cluster must alternate arrive and wait, and a wait completes
-// once every thread of the cluster that has not exited has arrived.
+// A cluster barrier in two halves, for work placed between them: every thread
+// of the cluster must alternate arrive (release) and wait (acquire), and a wait
+// completes once every thread of the cluster that has not exited has arrived.
 __device__ __forceinline__ void cluster_arrive_rel() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait_acq() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
@@ -141,11 +134,6 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t local, uint32_t rank)
     return r;
 }
 
-__device__ __forceinline__ void st_cluster_f32(uint32_t remote, float v)
-{
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
-}
-
 // An asynchronous store of one float into another CTA's shared memory whose
 // completion counts 4 transaction bytes on an mbarrier of that CTA (both
 // addresses from cluster_map): the data is visible to a thread that has seen
@@ -155,13 +143,6 @@ __device__ __forceinline__ void st_async_cluster_f32(uint32_t remote, float v, u
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(remote), "f"(v),
                  "r"(remote_bar)
                  : "memory");
-}
-
-// Arrives on an mbarrier of another CTA of the cluster, releasing this
-// thread's earlier memory operations at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
