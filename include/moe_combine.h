@@ -293,10 +293,10 @@ moe_status moe_combine(const moe_combine_args *args, moe_stream_t stream);
  *                  1..16 the largest thread-block cluster its single-launch
  *                  path may use;
  *   combine_split  CTAs that share one token's row, as a thread-block
- *                  cluster that splits the columns: 0 automatic (4 CTAs a
- *                  token while T * 4 <= the SM count and H >= 7168; with a
- *                  quantised output 2 while T * 2 <= the SM count and
- *                  H >= 7168; whole rows otherwise), 1 never, 2, 4, 8 or 16
+ *                  cluster that splits the columns: 0 automatic (for
+ *                  H >= 7168, 4 CTAs a token while T * 4 <= the SM count
+ *                  and 2 while T * 2 <= the SM count; whole rows
+ *                  otherwise), 1 never, 2, 4, 8 or 16
  *                  always where H allows it (slices of equal width holding
  *                  whole quant blocks, at most 4096 columns each; otherwise
  *                  whole rows).  vpt, rows_per_slot and ctas_per_sm apply

@@ -50,9 +50,9 @@
 //     meet through distributed shared memory: each warp sends its partial to
 //     every CTA of the cluster as an asynchronous store that completes on that
 //     CTA's mbarrier, and each CTA adds the partials in one fixed order.  This
-//     is the automatic plan for small batches (4 CTAs a token while T * 4 <=
-//     the SM count and H >= 7168; 2 for quantised output while T * 2 <= the
-//     SM count), where it halves or quarters one SM's copies and sums;
+//     is the automatic plan for small batches (at H >= 7168, 4 CTAs a token
+//     while T * 4 <= the SM count, 2 while T * 2 <= it), where it halves or
+//     quarters one SM's copies and sums;
 //   * gamma's slice is copied to shared memory once per CTA, and the
 //     per-warp partial sums of squares are added by a butterfly that gives
 //     every lane the same total.

@@ -283,10 +283,12 @@ __global__ void __launch_bounds__((max_consumer_warps<VPT>() + 1) * 32, 1) combi
     // with SPLIT, every CTA's barriers are initialised before any peer arrives
     // on them: each thread arrives on the cluster barrier here and waits on it
     // only before its first access to a peer's shared memory (the norm's
-    // exchange), so the barrier's latency hides behind the rows' copies
+    // exchange), so the barrier's latency hides behind the rows' copies.  The
+    // init was published by thread 0's fence_mbar_init, so the arrive is
+    // relaxed (a release here cost about 400 cycles)
     bool cl_waited = !SPLIT, cl_arrived2 = !SPLIT;
     if constexpr (SPLIT)
-        cluster_arrive_rel();
+        cluster_arrive_relaxed();
     // launched as a programmatic dependent: nothing before this line touches
     // global memory, so the setup above overlaps the previous kernel's tail
     grid_dependency_wait();
@@ -846,14 +848,14 @@ inline bool split_ok(int32_t H, int32_t quant, int c)
 // CTAs per token.  moe_tuning_set may ask for a cluster size (or 1, whole
 // rows); otherwise small batches split their rows over a thread-block cluster
 // while every CTA of it finds an SM of its own and keeps a slice of at least
-// 1792 columns: 4 CTAs a token up to sms / 4 tokens, and, with a quantised
-// output, 2 up to sms / 2 tokens; whole rows otherwise.  Measured on GB300
-// (graphs of 50 launches, k = 8, E = 256 / 128):
-//   H = 7168, residual + norm, bf16 out: T = 1: 4.28 us whole, 3.85 in 4s;
-//     T = 38: 4.43, 4.20 in 4s; T = 64: 4.46 whole, 4.58 in pairs;
-//   H = 7168, shared + residual + norm + MXFP8: T = 1: 5.42, 4.18 in 4s;
-//     T = 64: 5.62, 4.96 in pairs; T = 100: 5.74 whole, 9.40 in pairs;
-//   H = 4096, NVFP4: slower split from T = 32 (T = 64: 4.28 whole, 4.65 pairs).
+// 1792 columns: 4 CTAs a token up to sms / 4 tokens, 2 up to sms / 2; whole
+// rows otherwise.  Measured on GB300 (graphs of 50 launches, k = 8):
+//   H = 7168, residual + norm, bf16 out: T = 1: 4.34 us whole, 3.74 in 4s;
+//     T = 38: 4.42, 4.14 in 4s; T = 64: 4.47, 4.42 in pairs; T = 100: 4.59
+//     whole, 8.11 in pairs (more clusters than SMs);
+//   H = 7168, shared + residual + norm + MXFP8: T = 1: 5.45, 4.04 in 4s;
+//     T = 64: 5.61, 4.75 in pairs;
+//   H = 4096, NVFP4: no gain past T = 8 (T = 64: 4.30 whole, 4.42 in pairs).
 // A split token's CTAs each stage and sum a slice of every row, which halves
 // or quarters one SM's copy intake and consumer work; the slices' sums of
 // squares cost one exchange through distributed shared memory.
@@ -866,7 +868,7 @@ inline int choose_split(int32_t H, int64_t T, int32_t quant, int forced)
     const int64_t sms = sm_count();
     if (T * 4 <= sms && H / 4 >= 1792 && split_ok(H, quant, 4))
         return 4;
-    if (quant != MOE_QUANT_NONE && T * 2 <= sms && H / 2 >= 3584 && split_ok(H, quant, 2))
+    if (T * 2 <= sms && H / 2 >= 3584 && split_ok(H, quant, 2))
         return 2;
     return 1;
 }

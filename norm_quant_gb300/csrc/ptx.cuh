@@ -125,6 +125,9 @@ __device__ __forceinline__ uint32_t cluster_count_x()
 // completes once every thread of the cluster that has not exited has arrived.
 __device__ __forceinline__ void cluster_arrive_rel() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait_acq() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+// An arrive that orders nothing by itself: after fence_mbar_init it is the
+// pattern that publishes initialised barriers to the peers' acquiring waits.
+__device__ __forceinline__ void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory"); }
 
 // Address of the same shared-memory location in cluster CTA `rank`.
 __device__ __forceinline__ uint32_t cluster_map(uint32_t local, uint32_t rank)
