@@ -268,6 +268,28 @@ def test_bounded_wait_timeout_is_reported_and_the_context_survives():
     compare(wl, inp, orm, again)
 
 
+def test_split_rows_timeout_is_reported_and_the_context_survives():
+    """At decode sizes a token is split over a cluster.  The test hook stops
+    CTA 0's producer, so CTA 0's consumers give up on their first slot and
+    never send their partial sums; its peers send theirs and give up on the
+    exchange after 2 s.  Every thread still completes the cluster's
+    arrive-wait sequence, so the call ends, reports MOE_ERR_DEVICE_TIMEOUT,
+    and the next call on the same context is exact."""
+    wl = _wl(T=8, H=7168, k=8, E=256, outputs=("residual", "norm"))
+    assert nqg.moe_build_row_map_launches(wl.T, wl.k, wl.E) >= 1
+    inp = synth.make_inputs(wl)
+    d_rm, orm = route_and_check(inp["topk_ids"], wl.E)
+    try:
+        nqg.moe_debug_stall(0)
+        got = gpu_combine(wl, inp, d_rm)
+    finally:
+        nqg.moe_debug_stall(-1)
+    assert got["status"] == nqg.MOE_ERR_DEVICE_TIMEOUT
+    again = gpu_combine(wl, inp, d_rm, canary=True)
+    assert again["status"] == 0
+    compare(wl, inp, orm, again)
+
+
 def test_concurrent_calls_from_two_host_threads():
     """Two host threads call the combine at once, on their own streams, with
     workloads that need different shared-memory sizes (and so different
