@@ -41,6 +41,11 @@
  *  - All work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
  *    default stream) and returns without synchronising, except
  *    moe_build_row_map_check, which synchronises `stream`.
+ *  - Stream order holds as for any kernel.  The combine, the dispatch
+ *    permute and the single-launch routing builds are launched with
+ *    programmatic dependent launch: they may be scheduled while the previous
+ *    kernel on `stream` is still running, but they read and write global
+ *    memory only after it has completed and its writes are visible.
  *  - Arguments are validated on the host before anything is launched; an
  *    invalid call returns an error status and enqueues nothing.
  *  - A failed kernel launch returns MOE_ERR_CUDA.

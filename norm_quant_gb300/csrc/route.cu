@@ -29,6 +29,14 @@
 // kSmallMaxSlots slots use one CTA of 8 warps instead (route_small_kernel).
 // Cluster barriers are hardware barriers over co-scheduled CTAs, so nothing
 // spins.
+//
+// Both single-launch kernels are launched as programmatic dependents of the
+// previous kernel on the stream (typically the previous layer's combine,
+// which reads the row_map this build overwrites, or the router that writes
+// the ids).  They clear their shared histograms first and touch global
+// memory only after grid_dependency_wait, which returns once that kernel has
+// completed and its writes are visible; so their launch and set-up overlap
+// its tail.  The three-kernel path is launched plainly.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -344,6 +352,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     //    the count (the column is this warp's, so no atomics are needed)
     for (int e = lane; e < E; e += 32)
         hist[e * kHistPitch + warp] = 0;
+    grid_dependency_wait();  // nothing above touches global memory
     int32_t v[PL], rk[PL];
 #pragma unroll
     for (int it = 0; it < PL; ++it) {
@@ -554,6 +563,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     // 1. ranks within each warp's slots, counts in the warp's column
     for (int e = lane; e < E; e += 32)
         hist[e * kSmallPitch + warp] = 0;
+    grid_dependency_wait();  // nothing above touches global memory
     int32_t v[PL], rk[PL];
 #pragma unroll
     for (int it = 0; it < PL; ++it) {
@@ -562,23 +572,34 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     }
     const int key_bits = 32 - __clz(E);
     __syncwarp();
+    // the ballots of a lane's PL slots are independent, so they interleave
     bool bad = false;
+    uint32_t key[PL], peers[PL];
 #pragma unroll
     for (int it = 0; it < PL; ++it) {
         const int32_t e = v[it];
         const bool valid = e >= 0 && e < E;
         bad |= !valid && e != -1;
-        const uint32_t key = valid ? static_cast<uint32_t>(e) : static_cast<uint32_t>(E);
-        uint32_t peers = 0xffffffffu;
-        for (int b = 0; b < key_bits; ++b) {
-            const bool bit = (key >> b) & 1u;
+        key[it] = valid ? static_cast<uint32_t>(e) : static_cast<uint32_t>(E);
+        peers[it] = 0xffffffffu;
+    }
+    for (int b = 0; b < key_bits; ++b) {
+#pragma unroll
+        for (int it = 0; it < PL; ++it) {
+            const bool bit = (key[it] >> b) & 1u;
             const uint32_t on = __ballot_sync(0xffffffffu, bit);
-            peers &= bit ? on : ~on;
+            peers[it] &= bit ? on : ~on;
         }
-        rk[it] = valid ? hist[e * kSmallPitch + warp] + __popc(peers & lt) : 0;
+    }
+    // ranks and counts, slot by slot (the running count orders them)
+#pragma unroll
+    for (int it = 0; it < PL; ++it) {
+        const int32_t e = v[it];
+        const bool valid = e >= 0 && e < E;
+        rk[it] = valid ? hist[e * kSmallPitch + warp] + __popc(peers[it] & lt) : 0;
         __syncwarp();
-        if (valid && (peers & lt) == 0)
-            hist[e * kSmallPitch + warp] += __popc(peers);
+        if (valid && (peers[it] & lt) == 0)
+            hist[e * kSmallPitch + warp] += __popc(peers[it]);
         __syncwarp();
     }
     const int32_t any_bad = __syncthreads_or(bad ? 1 : 0);
@@ -610,24 +631,20 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     if (lane == 31)
         wsum[warp] = incl;
     __syncthreads();
-    if (warp == 0) {
-        const int32_t ws = lane < kSmallWarps ? wsum[lane] : 0;
-        int32_t wi = ws;
+    // every warp adds up the totals of the warps below it itself (8 reads of
+    // shared memory instead of one more barrier)
+    int32_t below = 0, total = 0;
 #pragma unroll
-        for (int d = 1; d < kSmallWarps; d <<= 1) {
-            const int32_t o = __shfl_up_sync(0xffffffffu, wi, d);
-            if (lane >= d)
-                wi += o;
-        }
-        if (lane < kSmallWarps)
-            wsum[lane] = wi - ws;
-        if (lane == kSmallWarps - 1) {
-            offsets[E] = wi;
-            *err = any_bad;
-        }
+    for (int w = 0; w < kSmallWarps; ++w) {
+        const int32_t x = wsum[w];
+        total += x;
+        below += (w < warp) ? x : 0;
     }
-    __syncthreads();
-    int32_t run = wsum[warp] + incl - s;
+    if (tid == 0) {
+        offsets[E] = total;
+        *err = any_bad;
+    }
+    int32_t run = below + incl - s;
     for (int e = ea; e < eb; ++e) {
         const int32_t c = off[e];
         counts[e] = c;
@@ -827,25 +844,36 @@ extern "C" moe_status moe_build_row_map(const int32_t *topk_ids, int64_t T, int3
             return MOE_ERR_CUDA;
         return MOE_OK;
     }
+    // the single-launch kernels go out as programmatic dependents (see the
+    // top of this file); a cluster dimension is added for a fused cluster
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (const int pl = small_plan(N, E)) {
-        small_fn(pl)<<<1, kSmallThreads, small_smem(E), s>>>(topk_ids, N, E, counts, offsets, row_map, src_row,
-                                                              err);
-        return launch_status();
+        cfg.gridDim = dim3(1);
+        cfg.blockDim = dim3(kSmallThreads);
+        cfg.dynamicSmemBytes = small_smem(E);
+        if (cudaLaunchKernelEx(&cfg, small_fn(pl), topk_ids, N, E, counts, offsets, row_map, src_row, err) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+        return MOE_OK;
     }
     FusedPlan f;
     if (fused_plan(N, E, &f)) {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = f.ctas;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = f.ctas;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
         cfg.gridDim = dim3(f.ctas);
         cfg.blockDim = dim3(kFusedThreads);
         cfg.dynamicSmemBytes = f.smem;
-        cfg.stream = s;
-        cfg.attrs = attr;
-        cfg.numAttrs = f.ctas > 1 ? 1 : 0;  // a lone CTA is launched as a plain kernel
+        cfg.numAttrs = f.ctas > 1 ? 2 : 1;  // a lone CTA is launched without a cluster
         if (cudaLaunchKernelEx(&cfg, fused_fn(f.per_lane), topk_ids, N, E, counts, offsets, row_map, src_row,
                                err) != cudaSuccess) {
             cudaGetLastError();

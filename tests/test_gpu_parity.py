@@ -17,7 +17,7 @@ import oracle
 from norm_quant_gb300 import synth
 from norm_quant_gb300.build import build
 
-from _helpers import (assert_bf16_close, assert_quant_close, d, dec16, gpu_combine, gpu_route, h,
+from _helpers import (DEV, assert_bf16_close, assert_quant_close, d, dec16, gpu_combine, gpu_route, h,
                       nvfp4_global_scale, oracle_combine, sum_magnitude)
 
 pytestmark = pytest.mark.gpu
@@ -340,6 +340,49 @@ def test_repeat_runs_identical_and_side_stream():
         b = gpu_combine(wl, inp, d_rm2, stream=s)
     for key in ("residual", "quant", "scales"):
         assert np.array_equal(a[key], b[key])
+
+
+@pytest.mark.parametrize("T", [64, 4096], ids=["one_cta_build", "cluster_build"])
+def test_consecutive_layers_on_one_stream(T):
+    """Two routings alternate on one stream, as consecutive MoE layers do: a
+    kernel writes each build's ids just before it, and each build overwrites
+    the row_map that the previous combine is reading.  Builds and combines are
+    launched as programmatic dependents of their predecessors, so their
+    launches overlap the previous kernel; neither order may break."""
+    wl = dataclasses.replace(synth.DECODE, T=T, name=f"layers_T{T}")
+    E, k, H = wl.E, wl.k, wl.H
+    inps = [synth.make_inputs(wl, seed=wl.seed + 11 * i) for i in range(2)]
+    key = 0x35A5A  # the ids are stored scrambled and restored by a kernel
+    enc = [d(inp["topk_ids"].astype(np.int32) ^ key) for inp in inps]
+    dev = [{n: d(inp[n]) for n in ("expert_out", "weights", "residual", "gamma")} for inp in inps]
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    row_map = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    ws = torch.zeros(nqg.moe_build_row_map_workspace_size(T, k, E), dtype=torch.uint8, device=DEV)
+    seq = [0, 1, 0, 1, 0, 1]
+    outs = [{n: torch.full((T, H), 0x5A5A, dtype=torch.int16, device=DEV) for n in ("residual", "norm")}
+            for _ in seq]
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for i, which in enumerate(seq):
+            torch.bitwise_xor(enc[which], key, out=ids)
+            nqg.moe_build_row_map(ids, E, counts, offsets, row_map, None, ws, stream=s.cuda_stream)
+            x = dev[which]
+            nqg.moe_combine(stream=s.cuda_stream, expert_out=x["expert_out"].reshape(-1, H), row_map=row_map,
+                            router_weights=x["weights"], residual=x["residual"], gamma=x["gamma"], eps=wl.eps,
+                            residual_out=outs[i]["residual"], norm_out=outs[i]["norm"], H=H)
+    torch.cuda.synchronize()
+    assert nqg.moe_build_row_map_check(ws) == nqg.MOE_OK
+    got = [{n: h(t, np.uint16) for n, t in o.items()} for o in outs]
+    for which in (0, 1):
+        _, _, _, orm, _ = oracle.build_row_map(inps[which]["topk_ids"], E)
+        compare(wl, inps[which], orm, got[which])
+    for i in range(2, len(seq)):
+        for n in ("residual", "norm"):
+            assert np.array_equal(got[i][n], got[i - 2][n]), f"call {i}: {n}"
+    assert not np.array_equal(got[0]["residual"], got[1]["residual"])
 
 
 @pytest.mark.parametrize("plan", [(1, 1, 0, 0), (1, 4, 0, 0), (2, 1, 0, 0), (2, 4, 32, 0), (4, 1, 0, 0),
