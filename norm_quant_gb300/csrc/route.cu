@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 }
 
 // Small builds (N <= kSmallMaxSlots, decode-sized batches): one CTA of 8
-// warps, launched as a plain kernel.  Warp w owns the PL * 32 consecutive
+// warps, launched without a cluster.  Warp w owns the PL * 32 consecutive
 // slots from w * PL * 32 and ranks them with ballots as above; one thread per
 // expert turns the 8 warp columns into exclusive prefixes and the expert's
 // count; a block scan over the experts gives the offsets.  The error word is
