@@ -50,7 +50,8 @@ KERNEL_SOURCES = ["norm_quant_gb300/csrc/combine.cu", "norm_quant_gb300/csrc/com
 # the committed ncu summary of each workload whose combine traffic was captured
 TRAFFIC_FILES = {"prefill": "profiles/combine_prefill_T4096_H7168_k8_mxfp8.md",
                  "fp16": "profiles/combine_prefill_fp16io_fp16weights_T4096_H7168_k8_mxfp8.md",
-                 "gemma": "profiles/combine_gemma_T8192_H4096_nvfp4_128x4.md"}
+                 "gemma": "profiles/combine_gemma_T8192_H4096_nvfp4_128x4.md",
+                 "decode": "profiles/combine_decode_T64_H7168_k8.md"}
 
 
 def parse():

@@ -80,14 +80,14 @@ def test_recorded_traffic_needs_a_matching_source_hash():
     h = bench.kernel_hash()
     summary = {f: f"x\ndram_bytes_per_launch: 123456\nkernel_source_hash: {h}\ncaptured: 2026-12-02\n"
                for f in bench.TRAFFIC_FILES.values()}
-    for kind in ("prefill", "fp16", "gemma"):
+    for kind in ("prefill", "fp16", "gemma", "decode"):
         got = bench.recorded_traffic(kind, summary.__getitem__)
         assert got["bytes"] == 123456 and got["kernel_source_hash"] == h and got["captured"] == "2026-12-02"
         assert got["file"] == bench.TRAFFIC_FILES[kind]
         prov = bench.traffic_provenance(kind, got)
         assert prov["file"] == got["file"] and prov["captured"] == "2026-12-02"
-    assert bench.recorded_traffic("decode", summary.__getitem__) is None
-    assert "no committed" in bench.traffic_provenance("decode", None)["how"]
+    assert bench.recorded_traffic("tiny", summary.__getitem__) is None
+    assert "no committed" in bench.traffic_provenance("tiny", None)["how"]
     stale = {f: t.replace(h, "0" * 16) for f, t in summary.items()}
     assert bench.recorded_traffic("prefill", stale.__getitem__) is None
     assert "other kernel source" in bench.traffic_provenance("prefill", None)["how"]
