@@ -342,13 +342,16 @@ def test_repeat_runs_identical_and_side_stream():
         assert np.array_equal(a[key], b[key])
 
 
+@pytest.mark.parametrize("mode", ["eager", "graph"])
 @pytest.mark.parametrize("T", [64, 4096], ids=["one_cta_build", "cluster_build"])
-def test_consecutive_layers_on_one_stream(T):
+def test_consecutive_layers_on_one_stream(T, mode):
     """Two routings alternate on one stream, as consecutive MoE layers do: a
     kernel writes each build's ids just before it, and each build overwrites
     the row_map that the previous combine is reading.  Builds and combines are
     launched as programmatic dependents of their predecessors, so their
-    launches overlap the previous kernel; neither order may break."""
+    launches overlap the previous kernel; neither order may break, launched
+    directly or replayed from a CUDA graph (where the dependencies become
+    programmatic graph edges)."""
     wl = dataclasses.replace(synth.DECODE, T=T, name=f"layers_T{T}")
     E, k, H = wl.E, wl.k, wl.H
     inps = [synth.make_inputs(wl, seed=wl.seed + 11 * i) for i in range(2)]
@@ -364,8 +367,8 @@ def test_consecutive_layers_on_one_stream(T):
     outs = [{n: torch.full((T, H), 0x5A5A, dtype=torch.int16, device=DEV) for n in ("residual", "norm")}
             for _ in seq]
     s = torch.cuda.Stream()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(s):
+
+    def layers():
         for i, which in enumerate(seq):
             torch.bitwise_xor(enc[which], key, out=ids)
             nqg.moe_build_row_map(ids, E, counts, offsets, row_map, None, ws, stream=s.cuda_stream)
@@ -373,6 +376,24 @@ def test_consecutive_layers_on_one_stream(T):
             nqg.moe_combine(stream=s.cuda_stream, expert_out=x["expert_out"].reshape(-1, H), row_map=row_map,
                             router_weights=x["weights"], residual=x["residual"], gamma=x["gamma"], eps=wl.eps,
                             residual_out=outs[i]["residual"], norm_out=outs[i]["norm"], H=H)
+
+    torch.cuda.synchronize()
+    if mode == "graph":
+        with torch.cuda.stream(s):
+            layers()  # the first calls configure the kernels, outside the capture
+        torch.cuda.synchronize()
+        for o in outs:
+            for t in o.values():
+                t.fill_(0x5A5A)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            layers()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            g.replay()
+    else:
+        with torch.cuda.stream(s):
+            layers()
     torch.cuda.synchronize()
     assert nqg.moe_build_row_map_check(ws) == nqg.MOE_OK
     got = [{n: h(t, np.uint16) for n, t in o.items()} for o in outs]
@@ -383,6 +404,66 @@ def test_consecutive_layers_on_one_stream(T):
         for n in ("residual", "norm"):
             assert np.array_equal(got[i][n], got[i - 2][n]), f"call {i}: {n}"
     assert not np.array_equal(got[0]["residual"], got[1]["residual"])
+
+
+@pytest.mark.parametrize("mode", ["eager", "graph"])
+@pytest.mark.parametrize("T", [64, 2048], ids=["one_cta_build", "cluster_build"])
+def test_layer_with_identity_experts(T, mode):
+    """A whole MoE layer on one stream with identity experts: the routing
+    build, the dispatch permute of the token rows, then the combine reading
+    the rows the permute has just written, each launch a programmatic
+    dependent of the one before.  The permuted rows must equal the oracle's
+    permute, and the combine's outputs the oracle's combine of those rows."""
+    wl = dataclasses.replace(synth.DECODE, T=T, name=f"identity_layer_T{T}")
+    E, k, H = wl.E, wl.k, wl.H
+    inp = synth.make_inputs(wl)
+    x = synth.bf16_normal(np.random.Generator(np.random.PCG64(T + 5)), (T, H))  # the token rows
+    _, _, oo, orm, _ = oracle.build_row_map(inp["topk_ids"], E)
+    nv = int(oo[E])
+    st, xg_want = oracle.dispatch_permute(x, orm, nv)
+    assert st == 0
+    d_ids, d_x, d_w, d_res, d_g = (d(a) for a in (inp["topk_ids"], x, inp["weights"], inp["residual"], inp["gamma"]))
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    row_map = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    ws = torch.zeros(nqg.moe_build_row_map_workspace_size(T, k, E), dtype=torch.uint8, device=DEV)
+    xg = torch.empty((nv, H), dtype=torch.int16, device=DEV)
+    outs = {n: torch.empty((T, H), dtype=torch.int16, device=DEV) for n in ("residual", "norm")}
+    s = torch.cuda.Stream()
+
+    def layer():
+        nqg.moe_build_row_map(d_ids, E, counts, offsets, row_map, None, ws, stream=s.cuda_stream)
+        nqg.moe_dispatch_permute(d_x, row_map, xg, stream=s.cuda_stream)
+        nqg.moe_combine(stream=s.cuda_stream, expert_out=xg, row_map=row_map, router_weights=d_w,
+                        residual=d_res, gamma=d_g, eps=wl.eps, residual_out=outs["residual"],
+                        norm_out=outs["norm"], H=H)
+
+    def clear():
+        for t in (row_map, xg, *outs.values()):
+            t.fill_(-1)
+
+    torch.cuda.synchronize()
+    if mode == "graph":
+        with torch.cuda.stream(s):
+            layer()  # the first calls configure the kernels, outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            layer()
+        clear()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            g.replay()
+    else:
+        clear()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            layer()
+    torch.cuda.synchronize()
+    assert nqg.moe_build_row_map_check(ws) == nqg.MOE_OK
+    assert np.array_equal(h(row_map), orm)
+    assert np.array_equal(h(xg, np.uint16), xg_want)
+    compare(wl, dict(inp, expert_out=xg_want, n_valid=nv), orm, {n: h(t, np.uint16) for n, t in outs.items()})
 
 
 @pytest.mark.parametrize("plan", [(1, 1, 0, 0), (1, 4, 0, 0), (2, 1, 0, 0), (2, 4, 32, 0), (4, 1, 0, 0),
