@@ -122,6 +122,11 @@ def _wl(**kw):
     dict(H=16, quant="nvfp4", outputs=("residual", "quant"), gamma_mean=0.0, weight_bias=1.0),
     dict(H=7200, T=19, quant="mxfp8", outputs=("residual", "norm", "quant")),   # ragged last slot
     dict(H=16384, T=9, k=8, E=32, quant="mxfp8", outputs=("residual", "quant")),  # largest H
+    # every limit at once (largest H, top_k and E): a few tokens (split over
+    # clusters), then enough for whole rows
+    dict(H=16384, T=5, k=32, E=8192, shared_std=0.5, quant="nvfp4", sf_layout="swizzled",
+         outputs=("residual", "norm", "quant")),
+    dict(H=16384, T=200, k=32, E=8192, quant="mxfp8", outputs=("combined", "residual", "norm", "quant")),
     dict(H=8192, T=13, quant="nvfp4", sf_layout="swizzled", outputs=("residual", "quant")),
     dict(H=96, T=130, quant="mxfp8", sf_layout="swizzled", outputs=("norm", "quant")),  # C = 3 pads
     dict(H=48, T=200, quant="nvfp4", sf_layout="swizzled", outputs=("combined", "quant")),
